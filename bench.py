@@ -1,0 +1,516 @@
+"""Benchmark of the GB300 block-quantized GEMV / MoE FFN hot path.
+
+One step = the dense batch-1 GEMV sweep: one 4096 x 4096 matrix per format
+(Q8_0, Q4_0, Q4_K, Q5_K, Q6_K, NaN scale in row 1), x ~ N(0,1), seed 0.
+`value` = algorithmic bytes of a step (weights + x + y) / device time, in
+GB/s, with inputs resident in HBM; weights rotate through copies totalling
+more than 4x the L2 so every step streams from HBM.  The same run measures
+the MoE FFN decode layer (128 experts, top-8, hidden 2048, expert_dim 768)
+in us/token, the dense SwiGLU FFN, and the 512-token MoE layer.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torch.distributed.run: each rank runs an independent
+replica (the path has no exchange step), timing is the max over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized GEMV weight GB/s & % of HBM peak; MoE FFN layer µs/token"
+FORMATS = [("Q8_0", 1), ("Q4_0", 2), ("Q4_K", 3), ("Q5_K", 4), ("Q6_K", 5)]
+ROWS = COLS = 4096
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_init(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if os.environ.get("QMOE_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device=None):
+    """Max of a float across ranks (all-reduce MAX); identity for one rank."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.rows = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) >= 9:
+                self.rows.append(f)
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows for k in range(4)
+                          if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, rank, world):
+    import torch
+
+    import moe_ffn_gb300 as qm
+    from moe_ffn_gb300 import synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qm.build()
+    qm.lib()
+    stream = torch.cuda.current_stream()
+
+    # ---- GEMV sweep: weights rotate over copies > 4x L2
+    mats, bytes_w = {}, {}
+    for name, qt in FORMATS:
+        g = synth.rng(qt)
+        W = synth.quant_matrix(g, qt, ROWS, COLS, nan_row=1)
+        x = synth.normal(g, COLS)
+        mats[name] = (qt, torch.from_numpy(W).to(dev), torch.from_numpy(x).to(dev))
+        bytes_w[name] = W.nbytes
+    set_bytes = sum(bytes_w.values())
+    n_copies = int(np.ceil(4 * L2_BYTES / set_bytes)) + 1
+    copies = {n: [mats[n][1].clone() for _ in range(n_copies)] for n, _ in FORMATS}
+    ys = {n: torch.empty(ROWS, device=dev) for n, _ in FORMATS}
+    torch.cuda.synchronize()
+    alg_step = sum(bytes_w[n] + 4 * COLS + 4 * ROWS for n, _ in FORMATS)
+
+    def step(i):
+        c = i % n_copies
+        for n, _ in FORMATS:
+            qt, _, x = mats[n]
+            qm.qmv(qt, copies[n][c], ROWS, COLS, x, ys[n], stream)
+
+    clk = Clocks(local).__enter__()  # sampled across all timed GPU work below
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_local = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(ms_local, world, dev)
+    ms_step = ms_total / args.steps
+    value = world * alg_step / (ms_step * 1e-3) / 1e9
+
+    # ---- per-format kernel timing (dominant kernel roofline): L launches
+    # back to back on the launching stream, rotating copies
+    peak, peak_kind = load_peaks()
+    per_fmt = {}
+    L = 60
+    for n, _ in FORMATS:
+        qt, _, x = mats[n]
+        for i in range(5):
+            qm.qmv(qt, copies[n][i % n_copies], ROWS, COLS, x, ys[n], stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(L):
+            qm.qmv(qt, copies[n][i % n_copies], ROWS, COLS, x, ys[n], stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / L
+        alg = bytes_w[n] + 4 * COLS + 4 * ROWS
+        per_fmt[n] = {"us": round(us, 3), "gbs": round(alg / us / 1e3, 1),
+                      "frac": round(alg / us / 1e3 / peak, 3), "bytes": alg}
+    dom = max(per_fmt, key=lambda n: per_fmt[n]["us"])
+    traffic = load_traffic(f"stream_gemv_{dom}")
+
+    # ---- end to end through the public API with host buffers
+    xs_host = {n: torch.from_numpy(synth.normal(synth.rng(100 + qt), COLS)).pin_memory()
+               for n, qt in FORMATS}
+    ys_host = {n: torch.empty(ROWS).pin_memory() for n, _ in FORMATS}
+    xs_dev = {n: torch.empty(COLS, device=dev) for n, _ in FORMATS}
+
+    def e2e_step(i):
+        c = i % n_copies
+        for n, _ in FORMATS:
+            qt = mats[n][0]
+            xs_dev[n].copy_(xs_host[n], non_blocking=True)
+            qm.qmv(qt, copies[n][c], ROWS, COLS, xs_dev[n], ys[n], stream)
+            ys_host[n].copy_(ys[n], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    e2e_value = world * alg_step / (e2e_ms * 1e-3) / 1e9
+
+    del copies
+    torch.cuda.empty_cache()
+    extra = {}
+    if not args.skip_layers:
+        extra = bench_layers(qm, synth, dev, stream, args)
+    clk.__exit__(None, None, None)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "dense batch-1 GEMV sweep, 4096x4096 per format "
+                               "Q8_0/Q4_0/Q4_K/Q5_K/Q6_K, NaN scale in row 1, seed 0",
+                   "rows": ROWS, "cols": COLS, "weight_copies": n_copies,
+                   "l2": "weights rotate over copies totalling > 4x L2 (no flush needed)",
+                   "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "hbm", "kernel": f"stream_gemv_kernel<{dom}, QMV>",
+                     "achieved": per_fmt[dom]["gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": per_fmt[dom]["frac"], "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
+        "per_format": per_fmt,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": 4 * COLS * len(FORMATS),
+                "d2h_bytes_per_step": 4 * ROWS * len(FORMATS)},
+        "gpu_launches": args.steps * len(FORMATS),
+        "clocks": clk.summary(),
+    }
+    line.update(extra)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+def load_traffic(key):
+    """dram bytes per launch from the committed ncu summary, if current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        v = d.get(key)
+        if isinstance(v, dict):
+            return v.get("bytes_per_launch")
+    return None
+
+
+def bench_layers(qm, synth, dev, stream, args):
+    """MoE decode (us/token), dense FFN (us/call), MoE 512-token layer (us/token)."""
+    import torch
+    out = {}
+    peak, _ = load_peaks()
+    # MoE decode: full stacks resident (391.6 MB > L2); x rotates over 64
+    # token vectors so the routing (and the experts read) varies per call.
+    shp = synth.MOE_DECODE
+    inp = synth.moe_inputs(0, **shp)
+    g = synth.rng(99)
+    xpool = torch.from_numpy(synth.normal(g, (64, shp["hidden"]))).to(dev)
+    s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"], 1,
+                     shp["gate"], shp["up"], shp["down"])
+    d = {k: torch.from_numpy(inp[k]).to(dev) for k in ("router", "gate", "up", "down")}
+    res = torch.from_numpy(inp["residual"]).to(dev)
+    ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device=dev)
+    idx = torch.empty((1, shp["top_k"]), dtype=torch.int32, device=dev)
+
+    def call(i):
+        qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, xpool[i % 64], res, idx, None,
+                   ws, stream=stream)
+    for i in range(10):
+        call(i)
+    torch.cuda.synchronize()
+    n = 200
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    rb_g = qm.row_bytes(shp["gate"], shp["hidden"])
+    rb_d = qm.row_bytes(shp["down"], shp["expert_dim"])
+    alg = (shp["num_experts"] * shp["hidden"] * 4
+           + shp["top_k"] * (2 * shp["expert_dim"] * rb_g + shp["hidden"] * rb_d)
+           + 3 * shp["hidden"] * 4)
+    out["moe_decode"] = {"us_per_token": round(us, 3), "alg_bytes": alg,
+                         "gbs": round(alg / us / 1e3, 1), "frac": round(alg / us / 1e3 / peak, 3),
+                         "launches_per_token": 3,
+                         "workload": "hidden 2048, 128 experts, top-8, expert_dim 768, Q4_K/Q4_K/Q6_K"}
+    del d, inp
+    torch.cuda.empty_cache()
+
+    # dense SwiGLU FFN: 114 MB weights, 5 copies rotating (> 4x L2)
+    w = synth.DENSE_FFN
+    fin = synth.ffn_inputs(0, **w)
+    ncp = 5
+    G = [torch.from_numpy(fin["gate"]).to(dev) for _ in range(ncp)]
+    U = [torch.from_numpy(fin["up"]).to(dev) for _ in range(ncp)]
+    D = [torch.from_numpy(fin["down"]).to(dev) for _ in range(ncp)]
+    x = torch.from_numpy(fin["x"]).to(dev)
+    r = torch.from_numpy(fin["residual"]).to(dev)
+    ws = torch.empty(qm.ffn_swiglu_workspace_size(w["hidden"], w["inter"]), dtype=torch.uint8,
+                     device=dev)
+
+    def fcall(i):
+        c = i % ncp
+        qm.ffn_swiglu(G[c], U[c], D[c], w["gate"], w["up"], w["down"], w["hidden"], w["inter"],
+                      x, r, ws, stream=stream)
+    for i in range(5):
+        fcall(i)
+    torch.cuda.synchronize()
+    n = 40
+    e0.record(stream)
+    for i in range(n):
+        fcall(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    alg = fin["gate"].nbytes + fin["up"].nbytes + fin["down"].nbytes + 4 * w["hidden"] * 3
+    out["dense_ffn"] = {"us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1),
+                        "frac": round(alg / us / 1e3 / peak, 3),
+                        "workload": "hidden 4096, intermediate 14336, Q4_K/Q4_K/Q6_K"}
+    del G, U, D
+    torch.cuda.empty_cache()
+
+    # MoE 512-token layer
+    shp = synth.MOE_PREFILL
+    inp = synth.moe_inputs(0, **shp)
+    s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"],
+                     shp["n_tokens"], shp["gate"], shp["up"], shp["down"])
+    d = {k: torch.from_numpy(inp[k]).to(dev) for k in ("router", "gate", "up", "down", "x",
+                                                          "residual")}
+    ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device=dev)
+
+    def pcall():
+        qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, d["x"], d["residual"], None,
+                   None, ws, stream=stream)
+    pcall()
+    torch.cuda.synchronize()
+    n = 3
+    e0.record(stream)
+    for _ in range(n):
+        pcall()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    out["moe_prefill"] = {"us_per_call": round(us, 1),
+                          "us_per_token": round(us / shp["n_tokens"], 3),
+                          "workload": "512 tokens, hidden 2048, 64 experts, top-8, "
+                                      "expert_dim 1024, Q4_K/Q4_K/Q6_K"}
+    return out
+
+
+# ------------------------------------------------------------- the oracle
+def oracle_sweep_setup():
+    import oracle
+    from moe_ffn_gb300 import synth
+    oracle.build()
+    data = []
+    for name, qt in FORMATS:
+        g = synth.rng(qt)
+        W = synth.quant_matrix(g, qt, ROWS, COLS, nan_row=1)
+        x = synth.normal(g, COLS)
+        data.append((qt, W, x))
+    return oracle, data
+
+
+def cpu_baseline(seconds=12.0, rows_sample=None):
+    """The oracle as it stands (plain C, one thread), timed on this host on
+    whole sweeps (all five 4096x4096 GEMVs) until `seconds` have passed."""
+    orc, data = oracle_sweep_setup()
+    alg = sum(W.nbytes + 4 * COLS + 4 * ROWS for _, W, _ in data)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        for qt, W, x in data:
+            orc.matvec(qt, W, ROWS, COLS, x)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n * alg / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full sweeps (5 x 4096x4096 GEMVs, decode-then-dot, fp64 "
+                      f"accumulation) in {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle, timed as the reference arm.  Each step is a bounded sample
+    of the sweep: one whole 4096x4096 GEMV, the five formats in turn (about
+    0.02 s of CPU work), so K steps take about K/50 s."""
+    orc, data = oracle_sweep_setup()
+    per = [W.nbytes + 4 * COLS + 4 * ROWS for _, W, _ in data]
+
+    def step(i):
+        qt, W, x = data[i % len(data)]
+        orc.matvec(qt, W, ROWS, COLS, x)
+        return per[i % len(data)]
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        done += step(i)
+    dt = time.perf_counter() - t0
+    ms_step = dt * 1e3 / args.steps
+    v = done / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "dense batch-1 GEMV sweep, 4096x4096 per format "
+                               "Q8_0/Q4_0/Q4_K/Q5_K/Q6_K, NaN scale in row 1, seed 0",
+                   "rows": ROWS, "cols": COLS, "parallelism": "replicas1"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} single-format 4096x4096 GEMVs (formats in turn) after {args.warmup} warm-up"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def run_profile_case(case, launches):
+    """Minimal program for ncu: one workload, `launches` calls, nothing else.
+    gemv:<FMT> — one 4096x4096 GEMV of that format; moe — the decode layer;
+    ffn — the dense FFN."""
+    import torch
+
+    import moe_ffn_gb300 as qm
+    from moe_ffn_gb300 import synth
+    qm.build()
+    dev = torch.device("cuda", 0)
+    if case.startswith("gemv:"):
+        name = case.split(":", 1)[1]
+        qt = dict(FORMATS)[name]
+        g = synth.rng(qt)
+        W = torch.from_numpy(synth.quant_matrix(g, qt, ROWS, COLS, nan_row=1)).to(dev)
+        x = torch.from_numpy(synth.normal(g, COLS)).to(dev)
+        y = torch.empty(ROWS, device=dev)
+        for _ in range(launches):
+            qm.qmv(qt, W, ROWS, COLS, x, y)
+    elif case == "moe":
+        shp = synth.MOE_DECODE
+        inp = synth.moe_inputs(0, **shp)
+        s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"], 1,
+                         shp["gate"], shp["up"], shp["down"])
+        d = {k: torch.from_numpy(inp[k]).to(dev) for k in inp}
+        ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device=dev)
+        for _ in range(launches):
+            qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, d["x"], d["residual"],
+                       None, None, ws)
+    elif case == "ffn":
+        w = synth.DENSE_FFN
+        fin = synth.ffn_inputs(0, **w)
+        d = {k: torch.from_numpy(fin[k]).to(dev) for k in fin}
+        ws = torch.empty(qm.ffn_swiglu_workspace_size(w["hidden"], w["inter"]),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(launches):
+            qm.ffn_swiglu(d["gate"], d["up"], d["down"], w["gate"], w["up"], w["down"],
+                          w["hidden"], w["inter"], d["x"], d["residual"], ws)
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    torch.cuda.synchronize()
+    st = qm.device_status()
+    print(json.dumps({"profile_case": case, "launches": launches, "device_status": st}))
+    return 0 if st == 0 else 1
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-layers", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile", default=None,
+                    help="run one small case for ncu (gemv:<FMT>, moe, ffn) and exit")
+    args = ap.parse_args(argv)
+    if args.profile:
+        return run_profile_case(args.profile, args.steps)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world = dist_init(args.gpus)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, 1)))
+        return 0
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

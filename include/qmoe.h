@@ -1,0 +1,169 @@
+/*
+ * qmoe.h — C ABI of the GB300 (sm_103a) GGUF block-quantized GEMV and
+ * decode-time MoE FFN library (libqmoe.so).
+ *
+ * Sources of the operations (page titles; the section is the Rust/CUDA item):
+ *   - "ferrox-cuda 0.14.0 — src/gpu.rs": the fused dequantize-and-dot matvec
+ *     kernels Q8_0/Q4_0/Q4_K/Q5_K/Q6_K_MATVEC_KERNEL_SRC and their launchers
+ *     launch_q*_matvec; SILU_MUL_KERNEL_SRC; launch_dense_ffn_swiglu;
+ *     CudaError (Unsupported is distinct from Launch: refuse, never compute
+ *     something else).
+ *   - "ferrox-core 0.16.0 — weight_matrix.rs": block_bytes_per_row,
+ *     apply (y = W x), apply_gpu_dense_ffn_swiglu (shape rules).
+ *   - "aprender-serve 0.70.2 — forward_qwen3_moe_resident.rs": module doc (MoE
+ *     op order, router weight folded into the SwiGLU activation), Qwen3MoeShape,
+ *     QuantWeight, ExpertStack (base + e * stride), check_moe_shape,
+ *     upload_experts, build_layer (F32 router), moe_layer, last_routes.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates nothing per call; scratch comes from the caller's workspace.
+ *   - Calls are asynchronous: they enqueue kernels on `stream` (a cudaStream_t
+ *     passed as void*; NULL = legacy default stream) and return without a host
+ *     synchronisation.  A status other than QMOE_OK means nothing was enqueued,
+ *     except QMOE_ERR_CUDA, which reports a failed launch.
+ *   - Weight operands (W, the router, the expert stacks) are read-only model
+ *     constants.  Kernels may start reading them before earlier kernels on the
+ *     same stream have finished (programmatic dependent launch), so weights
+ *     must be fully written (e.g. the upload synchronised) before the first
+ *     call that reads them.  Activations (x, residual, outputs, workspace) are
+ *     ordered by the stream as usual.
+ *   - Quantized matrices are row-major [rows][row_bytes] of little-endian ggml
+ *     blocks, row_bytes = cols / block_elems * block_bytes.  W must be 16-byte
+ *     aligned; the kernels read whole 16-byte granules that contain W's bytes
+ *     (never a byte outside those granules).
+ *   - Floating-point results are f32, accumulated in f32 with FMA; they match
+ *     the exact result within |err| <= 1e-3 * sum_j |w_ij x_j| + 1e-6 per GEMV
+ *     output, NaN where the exact computation is NaN (a NaN scale).  Non-finite
+ *     inputs (Inf scales, non-finite x) give non-finite outputs, NaN or Inf.
+ *   - Errors: the status names the class; qmoe_last_error() gives a message
+ *     (thread-local) naming the refused argument.
+ */
+#ifndef QMOE_H
+#define QMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight formats (the library's own numbering).  Block layouts are those of
+ * the kernel sources on "ferrox-cuda 0.14.0 — src/gpu.rs":
+ *   F32   4-byte floats (router / dense f32 GEMV)
+ *   Q8_0  34-byte blocks of 32: f16 d, int8 q[32]; value d*q
+ *   Q4_0  18-byte blocks of 32: f16 d, 16 bytes; byte i low nibble = element
+ *         i, high nibble = element i+16; value (nibble-8)*d
+ *   Q4_K  144-byte super-blocks of 256: f16 d, f16 dmin, 12 bytes of 6-bit
+ *         (scale, min) pairs, 128 bytes of nibbles; value (d*sc)*q - dmin*m
+ *   Q5_K  176-byte super-blocks: as Q4_K plus qh[32] giving each value a 5th bit
+ *   Q6_K  210-byte super-blocks: ql[128], qh[64], int8 scales[16], f16 d;
+ *         value (d*sc)*(q6-32) */
+typedef enum {
+    QMOE_F32 = 0,
+    QMOE_Q8_0 = 1,
+    QMOE_Q4_0 = 2,
+    QMOE_Q4_K = 3,
+    QMOE_Q5_K = 4,
+    QMOE_Q6_K = 5
+} qmoe_qtype;
+
+typedef enum {
+    QMOE_OK = 0,
+    QMOE_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misalignment, small workspace */
+    QMOE_ERR_UNSUPPORTED = 2,      /* valid request this library does not implement */
+    QMOE_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
+    QMOE_ERR_TIMEOUT = 4           /* a bounded device-side wait expired (qmoe_device_status) */
+} qmoe_status;
+
+/* MoE layer shape — Qwen3MoeShape (num_experts, num_experts_per_tok,
+ * expert_dim) plus the hidden size, token count and the stacks' formats. */
+typedef struct {
+    int32_t hidden;      /* H: model width; multiple of 256 */
+    int32_t expert_dim;  /* F: each expert's FFN width; multiple of 256 */
+    int32_t num_experts; /* E: 1..256 */
+    int32_t top_k;       /* k: 1..min(E, 16) */
+    int32_t n_tokens;    /* T >= 1 */
+    int32_t gate_qtype;  /* qmoe_qtype of the gate stack (quantized) */
+    int32_t up_qtype;    /* must equal gate_qtype */
+    int32_t down_qtype;  /* qmoe_qtype of the down stack (quantized) */
+} qmoe_moe_shape;
+
+/* y = W x — launch_q*_matvec on "ferrox-cuda 0.14.0 — src/gpu.rs" and
+ * WeightMatrix::apply on "ferrox-core 0.16.0 — weight_matrix.rs".
+ *   qtype  one of qmoe_qtype (F32 included: a plain f32 GEMV)
+ *   W      [rows][row_bytes] blocks, 16-byte aligned, read-only
+ *   rows   >= 1;  cols >= 1, a multiple of the format's block elements
+ *          (32 or 256; else INVALID_ARGUMENT) and, for quantized formats, of
+ *          256 (else UNSUPPORTED); cols <= 32768
+ *   x      [cols] f32, 16-byte aligned;  y [rows] f32, overwritten
+ * Errors: INVALID_ARGUMENT (null, sizes, alignment), UNSUPPORTED (qtype,
+ * cols, device not sm_103), CUDA. */
+qmoe_status qmv(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
+                void* stream);
+
+/* Bytes of workspace ffn_swiglu needs: inter f32 activations. */
+size_t ffn_swiglu_workspace_size(int64_t hidden, int64_t inter);
+
+/* residual += down( silu(gate x) * (up x) ) — launch_dense_ffn_swiglu on
+ * "ferrox-cuda 0.14.0 — src/gpu.rs" (gate, up, SwiGLU, down on device), with
+ * the result added to the residual as the MoE op order does for each expert
+ * (weight 1).  silu(g) = g / (1 + e^-g) (SILU_MUL_KERNEL_SRC).
+ *   gate, up   [inter][hidden] quantized, same qtype (else UNSUPPORTED)
+ *   down       [hidden][inter] quantized
+ *   hidden, inter  multiples of 256, <= 32768
+ *   x          [hidden] f32, the FFN input (after the norm)
+ *   residual   [hidden] f32, updated in place
+ *   ws         >= ffn_swiglu_workspace_size bytes of device memory, 16-byte
+ *              aligned; its contents are scratch
+ * Shape rules of apply_gpu_dense_ffn_swiglu (gate.cols == up.cols == x.len,
+ * down.cols == gate.rows) hold by construction of the arguments. */
+qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int gate_qtype,
+                       int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
+                       const float* x, float* residual, void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace moe_ffn needs for this shape. */
+size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
+
+/* The MoE FFN of one layer for T tokens — moe_layer on "aprender-serve
+ * 0.70.2 — forward_qwen3_moe_resident.rs", after ffn_norm:
+ *   logits = R x_t (F32 router [E][H]);  softmax over E, the top k (ties:
+ *   lower expert index), weights renormalised over those k;
+ *   for each routed (e, w) in rank order:  a = silu(G_e x_t) * (U_e x_t),
+ *   residual_t += D_e (w a).
+ * The routing runs on the device: no host synchronisation inside the layer.
+ *   router_W    [E][H] f32, 16-byte aligned
+ *   gate_stack, up_stack  [E][F][H] quantized, one allocation each; expert
+ *               e at base + e * F * row_bytes(H)  (ExpertStack::expert)
+ *   down_stack  [E][H][F] quantized
+ *   x           [T][H] f32 (normed input);  residual [T][H] f32, in place
+ *   topk_idx    [T][k] int32 or NULL: routed experts in rank order
+ *   topk_w      [T][k] f32 or NULL: their renormalised weights
+ *   ws          >= moe_ffn_workspace_size(shape) bytes, 16-byte aligned; scratch
+ * Errors: INVALID_ARGUMENT (null, shape fields out of range, k > E, small
+ * workspace, misalignment), UNSUPPORTED (E > 256, k > 16, F32 or mixed
+ * gate/up formats, sizes not multiples of 256), CUDA. */
+qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* up_stack,
+                    const void* down_stack, const qmoe_moe_shape* shape, const float* x,
+                    float* residual, int32_t* topk_idx, float* topk_w, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word: QMOE_ERR_TIMEOUT if a bounded device wait expired since the last
+ * read, QMOE_ERR_CUDA if the stream reported an error, else QMOE_OK. */
+qmoe_status qmoe_device_status(void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* qmoe_last_error(void);
+
+/* Row bytes of a [*][cols] matrix of this format (block_bytes_per_row on
+ * "ferrox-core 0.16.0 — weight_matrix.rs"); -1 if cols is not a whole number
+ * of blocks or the qtype is unknown. */
+int64_t qmoe_row_bytes(int qtype, int64_t cols);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMOE_H */

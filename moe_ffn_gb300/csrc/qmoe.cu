@@ -1,0 +1,537 @@
+// qmoe.cu — C-ABI entry points of libqmoe.so: argument validation, launch
+// planning and programmatic-dependent launches of the sm_103a kernels.
+// See include/qmoe.h for the contract of every function.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/qmoe.h"
+#include "formats.cuh"
+#include "ptx.cuh"
+#include "stream.cuh"
+
+namespace qmoe {
+
+// ----------------------------------------------------------------- errors
+static thread_local std::string g_last_error;
+
+static qmoe_status fail(qmoe_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+static qmoe_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(QMOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device error word (bounded waits record here).
+__device__ unsigned g_dev_err;
+
+// ------------------------------------------------------------ formats
+static int block_elems(int qt) {
+    switch (qt) {
+    case QT_F32: return 1;
+    case QT_Q8_0: case QT_Q4_0: return 32;
+    case QT_Q4_K: case QT_Q5_K: case QT_Q6_K: return 256;
+    default: return 0;
+    }
+}
+static int block_bytes(int qt) {
+    switch (qt) {
+    case QT_F32: return 4;
+    case QT_Q8_0: return 34;
+    case QT_Q4_0: return 18;
+    case QT_Q4_K: return 144;
+    case QT_Q5_K: return 176;
+    case QT_Q6_K: return 210;
+    default: return 0;
+    }
+}
+static int64_t row_bytes_of(int qt, int64_t cols) {
+    const int be = block_elems(qt);
+    if (be <= 0 || cols <= 0 || cols % be) return -1;
+    return cols / be * block_bytes(qt);
+}
+static const char* qname(int qt) {
+    switch (qt) {
+    case QT_F32: return "F32";
+    case QT_Q8_0: return "Q8_0";
+    case QT_Q4_0: return "Q4_0";
+    case QT_Q4_K: return "Q4_K";
+    case QT_Q5_K: return "Q5_K";
+    case QT_Q6_K: return "Q6_K";
+    default: return "unknown";
+    }
+}
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t MAX_K = 32768;
+
+// ------------------------------------------------------------ device info
+struct DevInfo {
+    bool init = false;
+    bool supported = false;
+    int sms = 0;
+    int smem_optin = 0;
+    unsigned* err = nullptr;
+    int cc_major = 0, cc_minor = 0;
+};
+static DevInfo g_dev[64];
+static std::mutex g_dev_mu;
+
+static qmoe_status device_info(DevInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(QMOE_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.init) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+        d.cc_major = prop.major;
+        d.cc_minor = prop.minor;
+        d.sms = prop.multiProcessorCount;
+        d.smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+        d.supported = (prop.major == 10 && prop.minor == 3);
+        if (d.supported) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_dev_err);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+            d.err = static_cast<unsigned*>(p);
+        }
+        d.init = true;
+    }
+    if (!d.supported)
+        return fail(QMOE_ERR_UNSUPPORTED,
+                    "device %d is compute capability %d.%d; this library is built for sm_103a "
+                    "(GB300) only",
+                    dev, d.cc_major, d.cc_minor);
+    *out = &d;
+    return QMOE_OK;
+}
+
+// ------------------------------------------------------------ launching
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Plan chunking and pipeline depth for a streamed GEMV; false if it cannot
+// fit in shared memory.
+template <class Fmt, int MODE>
+static bool plan(StreamParams& p, int smem_optin, int* smem_bytes) {
+    using G = ModeGeom<MODE>;
+    // stage budget: at most 48 KB, and at least two stages must fit beside
+    // the x' table
+    p.stage_bytes = 0;
+    p.nstages = 0;
+    const int room = smem_optin - smem_layout(p).total;
+    int budget = room / 2 < 48 * 1024 ? room / 2 : 48 * 1024;
+    if (budget < G::ROWS * (Fmt::SBB + 31)) return false;
+    const int seg_full = p.nb_seg * Fmt::SBB;
+    const int piece_full = align_up(seg_full + 15, 16);
+    int nbp_max;
+    if (G::ROWS * p.n_kseg * piece_full <= budget) {
+        p.n_sbc = 1;
+        p.chunk_ks = p.n_kseg;
+        p.chunk_sb = p.nb_seg;
+        nbp_max = p.nb_seg;
+    } else if (G::ROWS * piece_full <= budget) {
+        p.n_sbc = 1;
+        p.chunk_ks = budget / (G::ROWS * piece_full);
+        p.chunk_sb = p.nb_seg;
+        nbp_max = p.nb_seg;
+    } else {
+        p.chunk_ks = 1;
+        int csb = (budget / G::ROWS - 31) / Fmt::SBB;
+        if (csb >= G::WK) csb -= csb % G::WK;
+        if (csb < 1) csb = 1;
+        p.chunk_sb = csb;
+        p.n_sbc = (p.nb_seg + csb - 1) / csb;
+        nbp_max = csb;
+    }
+    p.piece_stride = align_up(nbp_max * Fmt::SBB + 15, 16);
+    p.slot_stride = p.chunk_ks * p.piece_stride;
+    if (p.slot_stride % 32 == 0) p.slot_stride += 16;  // alternate rows across bank halves
+    p.stage_bytes = G::ROWS * p.slot_stride;
+    p.n_chunk = (p.n_sbc == 1) ? (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks : p.n_kseg * p.n_sbc;
+    p.nstages = 0;
+    const int fixed = smem_layout(p).total;
+    int ns = (smem_optin - fixed) / p.stage_bytes;
+    if (ns > MAX_STAGES) ns = MAX_STAGES;
+    if (ns < 2) return false;
+    p.nstages = ns;
+    *smem_bytes = smem_layout(p).total;
+    return true;
+}
+
+template <class Fmt, int MODE>
+static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st) {
+    int smem = 0;
+    if (!plan<Fmt, MODE>(p, d.smem_optin, &smem))
+        return fail(QMOE_ERR_UNSUPPORTED,
+                    "K = %d x %d groups of 256 does not fit the shared-memory pipeline",
+                    p.n_kseg, p.nb_seg);
+    auto kern = stream_gemv_kernel<Fmt, MODE>;
+    static int configured_smem[64] = {};  // per instantiation and device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (smem > configured_smem[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        configured_smem[dev & 63] = smem;
+    }
+    p.err = d.err;
+    const int64_t grid = p.units < d.sms ? p.units : d.sms;
+    cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NTHREADS),
+                               static_cast<size_t>(smem), st, p);
+    if (e != cudaSuccess) return cuda_fail(e, "stream_gemv launch");
+    return QMOE_OK;
+}
+
+template <int MODE>
+static qmoe_status dispatch(int qt, const StreamParams& p, const DevInfo& d, cudaStream_t st) {
+    switch (qt) {
+    case QT_Q8_0: return run_stream<FmtQ80, MODE>(p, d, st);
+    case QT_Q4_0: return run_stream<FmtQ40, MODE>(p, d, st);
+    case QT_Q4_K: return run_stream<FmtQ4K, MODE>(p, d, st);
+    case QT_Q5_K: return run_stream<FmtQ5K, MODE>(p, d, st);
+    case QT_Q6_K: return run_stream<FmtQ6K, MODE>(p, d, st);
+    default: return fail(QMOE_ERR_UNSUPPORTED, "qtype %d has no streamed GEMV", qt);
+    }
+}
+
+// ------------------------------------------------------------ f32 GEMV
+// y[r] = R[r] . x for an f32 [rows][cols] matrix: one CTA of 128 threads
+// per row.  The router GEMV of the MoE layer and qmv(F32).  Weights are
+// loaded before the dependency wait.
+constexpr int F32_THREADS = 128;
+constexpr int F32_PREFETCH = 8;
+
+__global__ void __launch_bounds__(F32_THREADS) f32_gemv_kernel(const float* __restrict__ R,
+                                                               const float* __restrict__ x,
+                                                               float* __restrict__ y,
+                                                               int64_t cols) {
+    const int64_t r = blockIdx.x;
+    const int tid = threadIdx.x;
+    const float4* r4 = reinterpret_cast<const float4*>(R + r * cols);
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const int64_t n4 = cols / 4;
+    float4 w[F32_PREFETCH];
+#pragma unroll
+    for (int k = 0; k < F32_PREFETCH; ++k) {
+        const int64_t i = tid + static_cast<int64_t>(k) * F32_THREADS;
+        w[k] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
+    pdl_trigger();
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < F32_PREFETCH; ++k) {
+        const int64_t i = tid + static_cast<int64_t>(k) * F32_THREADS;
+        if (i < n4) {
+            const float4 xv = __ldcg(x4 + i);
+            acc = fmaf(w[k].x, xv.x, acc);
+            acc = fmaf(w[k].y, xv.y, acc);
+            acc = fmaf(w[k].z, xv.z, acc);
+            acc = fmaf(w[k].w, xv.w, acc);
+        }
+    }
+    for (int64_t i = tid + static_cast<int64_t>(F32_PREFETCH) * F32_THREADS; i < n4;
+         i += F32_THREADS) {
+        const float4 wv = __ldg(r4 + i), xv = __ldcg(x4 + i);
+        acc = fmaf(wv.x, xv.x, acc);
+        acc = fmaf(wv.y, xv.y, acc);
+        acc = fmaf(wv.z, xv.z, acc);
+        acc = fmaf(wv.w, xv.w, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    __shared__ float red[F32_THREADS / 32];
+    if ((tid & 31) == 0) red[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int k = 0; k < F32_THREADS / 32; ++k) s += red[k];
+        y[r] = s;
+    }
+}
+
+static qmoe_status run_f32_gemv(const float* R, const float* x, float* y, int64_t rows,
+                                int64_t cols, cudaStream_t st) {
+    cudaError_t e = launch_pdl(f32_gemv_kernel, dim3(static_cast<unsigned>(rows)),
+                               dim3(F32_THREADS), 0, st, R, x, y, cols);
+    if (e != cudaSuccess) return cuda_fail(e, "f32_gemv launch");
+    return QMOE_OK;
+}
+
+}  // namespace qmoe
+
+using namespace qmoe;
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* qmoe_last_error(void) { return g_last_error.c_str(); }
+
+int64_t qmoe_row_bytes(int qtype, int64_t cols) { return row_bytes_of(qtype, cols); }
+
+qmoe_status qmv(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
+                void* stream) {
+    g_last_error.clear();
+    if (qtype < QT_F32 || qtype > QT_Q6_K)
+        return fail(QMOE_ERR_UNSUPPORTED, "qmv: unknown qtype %d", qtype);
+    if (!W || !x || !y) return fail(QMOE_ERR_INVALID_ARGUMENT, "qmv: null pointer (W, x or y)");
+    if (rows <= 0 || cols <= 0)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "qmv: rows=%lld cols=%lld must be >= 1",
+                    (long long)rows, (long long)cols);
+    if (cols % block_elems(qtype))
+        return fail(QMOE_ERR_INVALID_ARGUMENT,
+                    "qmv: cols=%lld is not a whole number of %s blocks (%d elements)",
+                    (long long)cols, qname(qtype), block_elems(qtype));
+    if (qtype == QT_F32 ? (cols % 4 != 0) : (cols % 256 != 0))
+        return fail(QMOE_ERR_UNSUPPORTED,
+                    "qmv: cols=%lld must be a multiple of %d for %s on this path",
+                    (long long)cols, qtype == QT_F32 ? 4 : 256, qname(qtype));
+    if (cols > MAX_K)
+        return fail(QMOE_ERR_UNSUPPORTED, "qmv: cols=%lld exceeds %lld", (long long)cols,
+                    (long long)MAX_K);
+    if (rows > 0x7fffffffLL)
+        return fail(QMOE_ERR_UNSUPPORTED, "qmv: rows=%lld exceeds 2^31-1", (long long)rows);
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4))
+        return fail(QMOE_ERR_INVALID_ARGUMENT,
+                    "qmv: W and x must be 16-byte aligned, y 4-byte aligned");
+    DevInfo* d = nullptr;
+    if (qmoe_status s = device_info(&d)) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (qtype == QT_F32)
+        return run_f32_gemv(static_cast<const float*>(W), x, y, rows, cols, st);
+    StreamParams p = {};
+    p.units = rows;
+    p.nb_seg = static_cast<int>(cols / 256);
+    p.n_kseg = 1;
+    p.W0 = static_cast<const uint8_t*>(W);
+    p.rb0 = row_bytes_of(qtype, cols);
+    p.x = x;
+    p.out = y;
+    return dispatch<MODE_QMV>(qtype, p, *d, st);
+}
+
+size_t ffn_swiglu_workspace_size(int64_t hidden, int64_t inter) {
+    (void)hidden;
+    if (inter <= 0) return 0;
+    return static_cast<size_t>(align_up(static_cast<int>(inter * 4), 256));
+}
+
+static qmoe_status check_ffn_qtypes(const char* fn, int gq, int uq, int dq) {
+    for (int qt : {gq, uq, dq})
+        if (qt < QT_F32 || qt > QT_Q6_K) return fail(QMOE_ERR_UNSUPPORTED, "%s: unknown qtype %d", fn, qt);
+    if (gq == QT_F32 || uq == QT_F32 || dq == QT_F32)
+        return fail(QMOE_ERR_UNSUPPORTED, "%s: F32 gate/up/down weights are not implemented", fn);
+    if (gq != uq)
+        return fail(QMOE_ERR_UNSUPPORTED,
+                    "%s: gate (%s) and up (%s) must share a format (they are decoded by one "
+                    "kernel)",
+                    fn, qname(gq), qname(uq));
+    return QMOE_OK;
+}
+
+qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int gate_qtype,
+                       int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
+                       const float* x, float* residual, void* ws, size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (!gate || !up || !down || !x || !residual || !ws)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "ffn_swiglu: null pointer");
+    if (hidden <= 0 || inter <= 0)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "ffn_swiglu: hidden=%lld inter=%lld must be >= 1",
+                    (long long)hidden, (long long)inter);
+    if (qmoe_status s = check_ffn_qtypes("ffn_swiglu", gate_qtype, up_qtype, down_qtype)) return s;
+    if (hidden % block_elems(gate_qtype) || inter % block_elems(down_qtype))
+        return fail(QMOE_ERR_INVALID_ARGUMENT,
+                    "ffn_swiglu: hidden/inter not whole numbers of blocks");
+    if (hidden % 256 || inter % 256)
+        return fail(QMOE_ERR_UNSUPPORTED, "ffn_swiglu: hidden and inter must be multiples of 256");
+    if (hidden > MAX_K || inter > MAX_K)
+        return fail(QMOE_ERR_UNSUPPORTED, "ffn_swiglu: hidden/inter exceed %lld", (long long)MAX_K);
+    if (ws_bytes < ffn_swiglu_workspace_size(hidden, inter))
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "ffn_swiglu: workspace %zu < %zu bytes", ws_bytes,
+                    ffn_swiglu_workspace_size(hidden, inter));
+    if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(down, 16) || !aligned(x, 16) ||
+        !aligned(residual, 4) || !aligned(ws, 16))
+        return fail(QMOE_ERR_INVALID_ARGUMENT,
+                    "ffn_swiglu: weights, x and ws must be 16-byte aligned");
+    DevInfo* d = nullptr;
+    if (qmoe_status s = device_info(&d)) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* a = static_cast<float*>(ws);
+
+    StreamParams pg = {};
+    pg.units = inter;
+    pg.nb_seg = static_cast<int>(hidden / 256);
+    pg.n_kseg = 1;
+    pg.W0 = static_cast<const uint8_t*>(gate);
+    pg.rb0 = row_bytes_of(gate_qtype, hidden);
+    pg.W1 = static_cast<const uint8_t*>(up);
+    pg.rb1 = row_bytes_of(up_qtype, hidden);
+    pg.x = x;
+    pg.out = a;
+    if (qmoe_status s = dispatch<MODE_GATEUP>(gate_qtype, pg, *d, st)) return s;
+
+    StreamParams pd = {};
+    pd.units = hidden;
+    pd.nb_seg = static_cast<int>(inter / 256);
+    pd.n_kseg = 1;
+    pd.W0 = static_cast<const uint8_t*>(down);
+    pd.rb0 = row_bytes_of(down_qtype, inter);
+    pd.x = a;
+    pd.out = residual;
+    return dispatch<MODE_DOWN>(down_qtype, pd, *d, st);
+}
+
+static size_t moe_logits_bytes(const qmoe_moe_shape* s) {
+    return static_cast<size_t>(align_up(s->n_tokens * s->num_experts * 4, 256));
+}
+
+size_t moe_ffn_workspace_size(const qmoe_moe_shape* s) {
+    if (!s || s->n_tokens <= 0 || s->num_experts <= 0 || s->top_k <= 0 || s->expert_dim <= 0)
+        return 0;
+    return moe_logits_bytes(s) +
+           static_cast<size_t>(align_up(s->top_k * s->expert_dim * 4, 256));
+}
+
+qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* up_stack,
+                    const void* down_stack, const qmoe_moe_shape* shape, const float* x,
+                    float* residual, int32_t* topk_idx, float* topk_w, void* ws,
+                    size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (!shape) return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: null shape");
+    const qmoe_moe_shape s = *shape;
+    if (!router_W || !gate_stack || !up_stack || !down_stack || !x || !residual || !ws)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: null pointer");
+    // check_moe_shape: every count positive, k <= E
+    if (s.hidden <= 0 || s.expert_dim <= 0 || s.num_experts <= 0 || s.top_k <= 0 ||
+        s.n_tokens <= 0)
+        return fail(QMOE_ERR_INVALID_ARGUMENT,
+                    "moe_ffn: incomplete MoE shape (hidden=%d expert_dim=%d num_experts=%d "
+                    "top_k=%d n_tokens=%d)",
+                    s.hidden, s.expert_dim, s.num_experts, s.top_k, s.n_tokens);
+    if (s.top_k > s.num_experts)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: top_k=%d > num_experts=%d", s.top_k,
+                    s.num_experts);
+    if (qmoe_status st = check_ffn_qtypes("moe_ffn", s.gate_qtype, s.up_qtype, s.down_qtype))
+        return st;
+    if (s.num_experts > MAX_EXPERTS || s.top_k > MAX_TOPK)
+        return fail(QMOE_ERR_UNSUPPORTED,
+                    "moe_ffn: on-device routing supports num_experts <= %d and top_k <= %d",
+                    MAX_EXPERTS, MAX_TOPK);
+    if (s.hidden % block_elems(s.gate_qtype) || s.expert_dim % block_elems(s.down_qtype))
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: hidden/expert_dim not whole blocks");
+    if (s.hidden % 256 || s.expert_dim % 256)
+        return fail(QMOE_ERR_UNSUPPORTED, "moe_ffn: hidden and expert_dim must be multiples of 256");
+    if (s.hidden > MAX_K || static_cast<int64_t>(s.top_k) * s.expert_dim > MAX_K)
+        return fail(QMOE_ERR_UNSUPPORTED, "moe_ffn: hidden or top_k*expert_dim exceeds %lld",
+                    (long long)MAX_K);
+    if (ws_bytes < moe_ffn_workspace_size(&s))
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: workspace %zu < %zu bytes", ws_bytes,
+                    moe_ffn_workspace_size(&s));
+    if (!aligned(router_W, 16) || !aligned(gate_stack, 16) || !aligned(up_stack, 16) ||
+        !aligned(down_stack, 16) || !aligned(x, 16) || !aligned(residual, 4) || !aligned(ws, 16))
+        return fail(QMOE_ERR_INVALID_ARGUMENT,
+                    "moe_ffn: router, stacks, x and ws must be 16-byte aligned");
+    DevInfo* d = nullptr;
+    if (qmoe_status st = device_info(&d)) return st;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const int H = s.hidden, F = s.expert_dim, E = s.num_experts, K = s.top_k;
+    float* logits = static_cast<float*>(ws);
+    float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + moe_logits_bytes(&s));
+    const int64_t grb = row_bytes_of(s.gate_qtype, H), urb = row_bytes_of(s.up_qtype, H);
+    const int64_t drb = row_bytes_of(s.down_qtype, F);
+
+    for (int t = 0; t < s.n_tokens; ++t) {
+        const float* xt = x + static_cast<int64_t>(t) * H;
+        float* rt = residual + static_cast<int64_t>(t) * H;
+        float* lt = logits + static_cast<int64_t>(t) * E;
+        if (qmoe_status r = run_f32_gemv(router_W, xt, lt, E, H, st)) return r;
+
+        StreamParams pg = {};
+        pg.units = static_cast<int64_t>(K) * F;
+        pg.nb_seg = H / 256;
+        pg.n_kseg = 1;
+        pg.W0 = static_cast<const uint8_t*>(gate_stack);
+        pg.rb0 = grb;
+        pg.es0 = grb * F;
+        pg.W1 = static_cast<const uint8_t*>(up_stack);
+        pg.rb1 = urb;
+        pg.es1 = urb * F;
+        pg.x = xt;
+        pg.out = a;
+        pg.logits = lt;
+        pg.E = E;
+        pg.topk = K;
+        pg.F = F;
+        pg.topk_idx_out = topk_idx ? topk_idx + static_cast<int64_t>(t) * K : nullptr;
+        pg.topk_w_out = topk_w ? topk_w + static_cast<int64_t>(t) * K : nullptr;
+        pg.moe = 1;
+        if (qmoe_status r = dispatch<MODE_GATEUP>(s.gate_qtype, pg, *d, st)) return r;
+
+        StreamParams pd = {};
+        pd.units = H;
+        pd.nb_seg = F / 256;
+        pd.n_kseg = K;
+        pd.W0 = static_cast<const uint8_t*>(down_stack);
+        pd.rb0 = drb;
+        pd.es0 = drb * H;
+        pd.x = a;
+        pd.out = rt;
+        pd.logits = lt;
+        pd.E = E;
+        pd.topk = K;
+        pd.F = F;
+        pd.moe = 1;
+        if (qmoe_status r = dispatch<MODE_DOWN>(s.down_qtype, pd, *d, st)) return r;
+    }
+    return QMOE_OK;
+}
+
+qmoe_status qmoe_device_status(void* stream) {
+    g_last_error.clear();
+    DevInfo* d = nullptr;
+    if (qmoe_status s = device_info(&d)) return s;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned v = 0, zero = 0;
+    e = cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (v) {
+        e = cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        return fail(QMOE_ERR_TIMEOUT, "a bounded device wait expired (code %u: %s)", v,
+                    v == DEV_TIMEOUT_FULL ? "stage never filled" : "stage never released");
+    }
+    return QMOE_OK;
+}
+
+}  // extern "C"

@@ -73,7 +73,7 @@ def _load():
             lib.orc_route.restype = ctypes.c_int
             lib.orc_route.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P]
             lib.orc_moe_ffn.restype = ctypes.c_int
-            lib.orc_moe_ffn.argtypes = [P, i64, P, P, P, P, P, P, P, P, P, P, P]
+            lib.orc_moe_ffn.argtypes = [P, i64, P, P, P, P, P, P, P, P, P, P, P, P, P]
             lib.orc_ffn_swiglu.restype = ctypes.c_int
             lib.orc_ffn_swiglu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, i64,
                                            P, P, P, P, P, P, P]
@@ -173,7 +173,8 @@ def moe_ffn(hidden, expert_dim, num_experts, top_k, gate_qt, up_qt, down_qt,
     """MoE FFN per token.  x, residual: [T][hidden].  ``tokens`` (optional)
     restricts the computation to those token rows (sampled checks).
 
-    Returns dict(out [T'][hidden] f64, tol, idx [T'][k], w [T'][k], gap [T'])."""
+    Returns dict(out [T'][hidden] f64, tol, idx [T'][k], w [T'][k], gap [T'],
+    logits [T'][E], lscale [T'] = max_e sum_j |R_ej x_j|)."""
     x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, hidden)
     residual = np.ascontiguousarray(residual, dtype=np.float32).reshape(-1, hidden)
     if tokens is not None:
@@ -188,12 +189,14 @@ def moe_ffn(hidden, expert_dim, num_experts, top_k, gate_qt, up_qt, down_qt,
     idx = np.zeros((T, top_k), np.int32)
     w = np.zeros((T, top_k), np.float64)
     gap = np.zeros(T, np.float64)
+    logits = np.zeros((T, num_experts), np.float64)
+    lscale = np.zeros(T, np.float64)
     rc = _load().orc_moe_ffn(ctypes.byref(sh), T, _ptr(router), _ptr(_u8(gate)), _ptr(_u8(up)),
                              _ptr(_u8(down)), _ptr(x), _ptr(residual), _ptr(out), _ptr(tol),
-                             _ptr(idx), _ptr(w), _ptr(gap))
+                             _ptr(idx), _ptr(w), _ptr(gap), _ptr(logits), _ptr(lscale))
     if rc != 0:
         raise ValueError(f"orc_moe_ffn rejected the shape (rc={rc})")
-    return dict(out=out, tol=tol, idx=idx, w=w, gap=gap)
+    return dict(out=out, tol=tol, idx=idx, w=w, gap=gap, logits=logits, lscale=lscale)
 
 
 def ffn_swiglu(gate_qt, up_qt, down_qt, hidden, inter, gate, up, down, x, residual):

@@ -360,7 +360,9 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
  *   (dw_s/dl_t = w_s (delta_st - w_t), so |dw_s| <= 2 w_s (1 - w_s) max |dl|).
  * route_idx/route_w (nullable) receive [T][k]; logit_gap (nullable)
  * receives per token the smallest gap among the top k+1 sorted logits
- * divided by max_t sum_j |R_tj x_j| (the ambiguity measure for ties). */
+ * divided by max_t sum_j |R_tj x_j| (the ambiguity measure for ties);
+ * logits_out / lscale_out (nullable) receive [T][E] logits and per token
+ * max_t sum_j |R_tj x_j|. */
 typedef struct {
     int32_t hidden, expert_dim, num_experts, top_k;
     int32_t gate_qt, up_qt, down_qt;
@@ -374,7 +376,7 @@ static double dsilu(double g) {
 int orc_moe_ffn(const orc_moe_shape *sh, int64_t T, const float *router, const uint8_t *gate,
                 const uint8_t *up, const uint8_t *down, const float *x, const float *residual,
                 double *out, double *tol, int32_t *route_idx, double *route_w,
-                double *logit_gap) {
+                double *logit_gap, double *logits_out, double *lscale_out) {
     int H = sh->hidden, F = sh->expert_dim, E = sh->num_experts, K = sh->top_k;
     if (H <= 0 || F <= 0 || E <= 0 || K <= 0 || K > E) return -1;
     int64_t grb = orc_row_bytes(sh->gate_qt, H), urb = orc_row_bytes(sh->up_qt, H);
@@ -414,6 +416,13 @@ int orc_moe_ffn(const orc_moe_shape *sh, int64_t T, const float *router, const u
             if (d > dl) dl = d;
         }
         orc_route(logits, E, K, idx, w);
+        if (logits_out)
+            for (int e = 0; e < E; e++) logits_out[t * E + e] = logits[e];
+        if (lscale_out) {
+            double mx = 0.0;
+            for (int e = 0; e < E; e++) if (lab[e] > mx) mx = lab[e];
+            lscale_out[t] = mx;
+        }
         if (route_idx)
             for (int s = 0; s < K; s++) route_idx[t * K + s] = idx[s];
         if (route_w)

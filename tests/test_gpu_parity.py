@@ -1,0 +1,205 @@
+"""GPU parity: the CUDA library (called through the C ABI) against the CPU
+oracle on the same seeded inputs — element by element at sizes that span
+several tiles and a ragged tail, and at the workloads' full sizes."""
+import numpy as np
+import pytest
+
+from moe_ffn_gb300 import synth
+from tests.parity import AMBIGUITY, check_close, check_gemv, check_moe, route_is_valid
+
+pytestmark = pytest.mark.gpu
+
+QTS = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q5_K, synth.Q6_K]
+QNAME = {1: "Q8_0", 2: "Q4_0", 3: "Q4_K", 4: "Q5_K", 5: "Q6_K", 0: "F32"}
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_qmv(qm, qt, W, rows, cols, x):
+    import torch
+    Wd, xd = _dev(W), _dev(x)
+    y = torch.full((rows,), float("nan"), device="cuda")
+    qm.qmv(qt, Wd, rows, cols, xd, y)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("qt", QTS, ids=lambda q: QNAME[q])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (7, 256), (37, 768), (300, 1024),
+                                       (153, 4096), (64, 14336), (9, 32768)])
+def test_qmv_small(qm, orc, qt, rows, cols):
+    g = synth.rng(1000 + qt * 7 + rows)
+    W = synth.quant_matrix(g, qt, rows, cols, nan_row=rows // 2 if rows > 2 else None)
+    x = synth.normal(g, cols)
+    y = gpu_qmv(qm, qt, W, rows, cols, x)
+    ref, sabs = orc.matvec(qt, W, rows, cols, x, with_sabs=True)
+    check_gemv(y, ref, sabs, f"qmv {QNAME[qt]} {rows}x{cols}")
+
+
+def test_qmv_f32(qm, orc):
+    g = synth.rng(5)
+    rows, cols = 129, 2048
+    R = synth.normal(g, (rows, cols), 0.02)
+    x = synth.normal(g, cols)
+    y = gpu_qmv(qm, synth.F32, R, rows, cols, x)
+    ref, sabs = orc.matvec(orc.F32, R.view(np.uint8), rows, cols, x, with_sabs=True)
+    check_gemv(y, ref, sabs, "qmv F32")
+
+
+def test_qmv_single_q4_0_workload(qm, orc):
+    """256 x 1024 Q4_0, d ~ U(1e-3, 1e-2), uniform nibbles, x ~ N(0,1), seed 0."""
+    w = synth.GEMV_SMALL
+    g = synth.rng(0)
+    W = synth.quant_matrix(g, w["qtype"], w["rows"], w["cols"])
+    x = synth.normal(g, w["cols"])
+    y = gpu_qmv(qm, w["qtype"], W, w["rows"], w["cols"], x)
+    ref, sabs = orc.matvec(w["qtype"], W, w["rows"], w["cols"], x, with_sabs=True)
+    check_gemv(y, ref, sabs, "Q4_0 256x1024")
+
+
+@pytest.mark.parametrize("qt", QTS, ids=lambda q: QNAME[q])
+def test_qmv_sweep_workload(qm, orc, qt):
+    """4096 x 4096 per format, NaN f16 scale in block 0 of row 1."""
+    w = synth.GEMV_SWEEP
+    g = synth.rng(qt)
+    W = synth.quant_matrix(g, qt, w["rows"], w["cols"], nan_row=w["nan_row"])
+    x = synth.normal(g, w["cols"])
+    y = gpu_qmv(qm, qt, W, w["rows"], w["cols"], x)
+    ref, sabs = orc.matvec(qt, W, w["rows"], w["cols"], x, with_sabs=True)
+    assert np.isnan(ref[1]) and np.isnan(y[1])
+    check_gemv(y, ref, sabs, f"sweep {QNAME[qt]}")
+
+
+def test_qmv_repeatable_and_in_stream_order(qm, orc):
+    """Back-to-back calls on one stream with a dependent x: y2 = W (y1[:cols])."""
+    import torch
+    g = synth.rng(77)
+    rows = cols = 1024
+    W = synth.quant_matrix(g, synth.Q4_K, rows, cols)
+    x = synth.normal(g, cols)
+    Wd, xd = _dev(W), _dev(x)
+    y1 = torch.empty(rows, device="cuda")
+    y2 = torch.empty(rows, device="cuda")
+    for _ in range(3):
+        qm.qmv(synth.Q4_K, Wd, rows, cols, xd, y1)
+        qm.qmv(synth.Q4_K, Wd, rows, cols, y1, y2)
+    torch.cuda.synchronize()
+    r1 = orc.matvec(synth.Q4_K, W, rows, cols, x)
+    r2, s2 = orc.matvec(synth.Q4_K, W, rows, cols, y1.cpu().numpy(), with_sabs=True)
+    check_gemv(y2.cpu().numpy(), r2, s2, "chained")
+    assert np.allclose(y1.cpu().numpy(), r1, rtol=1e-3, atol=1e-3)
+    assert qm.device_status() == qm.OK
+
+
+# ------------------------------------------------------------- dense FFN
+def gpu_ffn(qm, inp, H, F, gq, uq, dq):
+    import torch
+    res = _dev(inp["residual"])
+    ws = torch.empty(qm.ffn_swiglu_workspace_size(H, F), dtype=torch.uint8, device="cuda")
+    qm.ffn_swiglu(_dev(inp["gate"]), _dev(inp["up"]), _dev(inp["down"]), gq, uq, dq, H, F,
+                  _dev(inp["x"]), res, ws)
+    torch.cuda.synchronize()
+    return res.cpu().numpy()
+
+
+@pytest.mark.parametrize("H,F,gq,dq", [(256, 512, synth.Q4_K, synth.Q6_K),
+                                       (512, 768, synth.Q8_0, synth.Q4_0),
+                                       (768, 256, synth.Q5_K, synth.Q8_0),
+                                       (1024, 2048, synth.Q4_0, synth.Q5_K)])
+def test_ffn_small(qm, orc, H, F, gq, dq):
+    inp = synth.ffn_inputs(H + F, hidden=H, inter=F, gate=gq, up=gq, down=dq)
+    got = gpu_ffn(qm, inp, H, F, gq, gq, dq)
+    ref, tol = orc.ffn_swiglu(gq, gq, dq, H, F, inp["gate"], inp["up"], inp["down"], inp["x"],
+                              inp["residual"])
+    check_close(got, ref, tol, f"ffn {H}x{F}")
+
+
+def test_ffn_dense_workload(qm, orc):
+    """hidden 4096, intermediate 14336, gate/up Q4_K, down Q6_K."""
+    w = synth.DENSE_FFN
+    inp = synth.ffn_inputs(0, **w)
+    got = gpu_ffn(qm, inp, w["hidden"], w["inter"], w["gate"], w["up"], w["down"])
+    ref, tol = orc.ffn_swiglu(w["gate"], w["up"], w["down"], w["hidden"], w["inter"],
+                              inp["gate"], inp["up"], inp["down"], inp["x"], inp["residual"])
+    check_close(got, ref, tol, "dense ffn")
+
+
+# ------------------------------------------------------------------ MoE
+def gpu_moe(qm, inp, shp):
+    import torch
+    T, K = shp["n_tokens"], shp["top_k"]
+    s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], K, T,
+                     shp["gate"], shp["up"], shp["down"])
+    res = _dev(inp["residual"])
+    idx = torch.full((T, K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, K), device="cuda")
+    ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device="cuda")
+    qm.moe_ffn(_dev(inp["router"]), _dev(inp["gate"]), _dev(inp["up"]), _dev(inp["down"]), s,
+               _dev(inp["x"]), res, idx, w, ws)
+    torch.cuda.synchronize()
+    return res.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def oracle_moe(orc, inp, shp, tokens=None):
+    return orc.moe_ffn(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"],
+                       shp["gate"], shp["up"], shp["down"], inp["router"], inp["gate"],
+                       inp["up"], inp["down"], inp["x"], inp["residual"], tokens=tokens)
+
+
+MOE_SMALL = [
+    dict(hidden=256, expert_dim=256, num_experts=6, top_k=2, n_tokens=3),
+    dict(hidden=512, expert_dim=512, num_experts=1, top_k=1, n_tokens=1),
+    dict(hidden=256, expert_dim=768, num_experts=4, top_k=4, n_tokens=2),
+    dict(hidden=1024, expert_dim=256, num_experts=40, top_k=16, n_tokens=1),
+    dict(hidden=768, expert_dim=512, num_experts=256, top_k=3, n_tokens=2),
+]
+
+
+@pytest.mark.parametrize("shp", MOE_SMALL, ids=lambda s: "E{num_experts}k{top_k}T{n_tokens}".format(**s))
+@pytest.mark.parametrize("fmts", [(synth.Q4_K, synth.Q6_K), (synth.Q8_0, synth.Q4_0),
+                                  (synth.Q5_K, synth.Q4_K)], ids=lambda f: f"{QNAME[f[0]]}-{QNAME[f[1]]}")
+def test_moe_small(qm, orc, shp, fmts):
+    shp = dict(shp, gate=fmts[0], up=fmts[0], down=fmts[1])
+    inp = synth.moe_inputs(31 + shp["num_experts"], **shp)
+    out, idx, w = gpu_moe(qm, inp, shp)
+    ref = oracle_moe(orc, inp, shp)
+    assert check_moe(out, idx, w, ref) <= 1
+
+
+def test_moe_decode_workload(qm, orc):
+    """Qwen3-30B-A3B-shaped: hidden 2048, 128 experts, top-8, expert_dim 768."""
+    shp = synth.MOE_DECODE
+    inp = synth.moe_inputs(0, **shp)
+    out, idx, w = gpu_moe(qm, inp, shp)
+    ref = oracle_moe(orc, inp, shp)
+    assert check_moe(out, idx, w, ref) == 0
+
+
+def test_moe_prefill_workload_sampled(qm, orc):
+    """OLMoE-shaped, 512 tokens: every token's routing checked exactly;
+    residuals of 12 sampled tokens checked against the oracle."""
+    shp = synth.MOE_PREFILL
+    inp = synth.moe_inputs(0, **shp)
+    out, idx, w = gpu_moe(qm, inp, shp)
+    toks = np.array([0, 1, 2, 63, 64, 127, 200, 255, 256, 384, 510, 511])
+    ref = oracle_moe(orc, inp, shp, tokens=toks)
+    assert check_moe(out[toks], idx[toks], w[toks], ref) <= 2
+    # routing of all tokens: exact top-k wherever the oracle's logits are
+    # unambiguous, a valid top-k elsewhere
+    K = shp["top_k"]
+    R64, X64 = inp["router"].astype(np.float64), inp["x"].astype(np.float64)
+    logits = X64 @ R64.T
+    scales = (np.abs(X64) @ np.abs(R64).T).max(axis=1)
+    mismatched = 0
+    for t in range(shp["n_tokens"]):
+        ri, _ = orc.route(logits[t], K)
+        srt = np.sort(logits[t])[::-1][: K + 1]
+        if np.min(-np.diff(srt)) > AMBIGUITY * scales[t]:
+            assert list(idx[t]) == list(ri), t
+        else:
+            assert route_is_valid(idx[t], logits[t], scales[t], K), t
+            mismatched += list(idx[t]) != list(ri)
+    assert mismatched <= 5
