@@ -150,50 +150,49 @@ def run_ours(args, rank, world):
         c = i % n_copies
         for n, _ in FORMATS:
             qt, _, x = mats[n]
-            qm.qmv(qt, copies[n][c], ROWS, COLS, x, ys[n], stream)
+            qm.qmv(qt, copies[n][c], ROWS, COLS, x, ys[n])
 
+    # One graph holds n_copies steps (every copy once); the timed region
+    # replays it.  Launch cost is paid at capture, as a serving loop would.
     clk = Clocks(local).__enter__()  # sampled across all timed GPU work below
-    for i in range(args.warmup):
-        step(i)
+    g_sweep = capture(torch, step, n_copies)
+    replays = max(1, args.steps // n_copies)
+    steps_timed = replays * n_copies
+    for _ in range(max(1, args.warmup // n_copies + 1)):
+        g_sweep.replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms_local = time_replays(torch, g_sweep, replays)
     barrier(world)
-    ms_local = ev0.elapsed_time(ev1)
     ms_total = max_over_ranks(ms_local, world, dev)
-    ms_step = ms_total / args.steps
+    ms_step = ms_total / steps_timed
     value = world * alg_step / (ms_step * 1e-3) / 1e9
 
     # ---- per-format kernel timing (dominant kernel roofline): L launches
-    # back to back on the launching stream, rotating copies
+    # back to back in a graph on the launching stream, rotating copies
     peak, peak_kind = load_peaks()
     per_fmt = {}
-    L = 60
+    L = 4 * n_copies
     for n, _ in FORMATS:
         qt, _, x = mats[n]
-        for i in range(5):
-            qm.qmv(qt, copies[n][i % n_copies], ROWS, COLS, x, ys[n], stream)
+
+        def one(i, qt=qt, n=n, x=x):
+            qm.qmv(qt, copies[n][i % n_copies], ROWS, COLS, x, ys[n])
+        gf = capture(torch, one, L)
+        gf.replay()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(L):
-            qm.qmv(qt, copies[n][i % n_copies], ROWS, COLS, x, ys[n], stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / L
+        us = time_replays(torch, gf, 5) * 1e3 / (5 * L)
         alg = bytes_w[n] + 4 * COLS + 4 * ROWS
         per_fmt[n] = {"us": round(us, 3), "gbs": round(alg / us / 1e3, 1),
                       "frac": round(alg / us / 1e3 / peak, 3), "bytes": alg}
+        del gf
     dom = max(per_fmt, key=lambda n: per_fmt[n]["us"])
     traffic = load_traffic(f"stream_gemv_{dom}")
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # copies x from pinned host memory, runs the five GEMVs and copies y
+    # back; plain calls from Python, no graph.
     xs_host = {n: torch.from_numpy(synth.normal(synth.rng(100 + qt), COLS)).pin_memory()
                for n, qt in FORMATS}
     ys_host = {n: torch.empty(ROWS).pin_memory() for n, _ in FORMATS}
@@ -207,21 +206,22 @@ def run_ours(args, rank, world):
             qm.qmv(qt, copies[n][c], ROWS, COLS, xs_dev[n], ys[n], stream)
             ys_host[n].copy_(ys[n], non_blocking=True)
 
+    e2e_steps = min(args.steps, 500)
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
+    for i in range(e2e_steps):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
     e2e_value = world * alg_step / (e2e_ms * 1e-3) / 1e9
 
-    del copies
+    del copies, g_sweep
     torch.cuda.empty_cache()
     extra = {}
     if not args.skip_layers:
@@ -230,13 +230,14 @@ def run_ours(args, rank, world):
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "steps": steps_timed, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": "dense batch-1 GEMV sweep, 4096x4096 per format "
                                "Q8_0/Q4_0/Q4_K/Q5_K/Q6_K, NaN scale in row 1, seed 0",
                    "rows": ROWS, "cols": COLS, "weight_copies": n_copies,
                    "l2": "weights rotate over copies totalling > 4x L2 (no flush needed)",
+                   "launch": f"CUDA graph of {n_copies} steps, replayed",
                    "parallelism": f"replicas{world}"},
         "roofline": {"bound": "hbm", "kernel": f"stream_gemv_kernel<{dom}, QMV>",
                      "achieved": per_fmt[dom]["gbs"], "peak": peak, "unit": "GB/s",
@@ -245,14 +246,45 @@ def run_ours(args, rank, world):
         "per_format": per_fmt,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": 4 * COLS * len(FORMATS),
-                "d2h_bytes_per_step": 4 * ROWS * len(FORMATS)},
-        "gpu_launches": args.steps * len(FORMATS),
+                "d2h_bytes_per_step": 4 * ROWS * len(FORMATS),
+                "how": "plain Python calls per step (no graph), pinned-host x in, y out"},
+        "gpu_launches": steps_timed * len(FORMATS),
         "clocks": clk.summary(),
     }
     line.update(extra)
     if rank == 0 and world == 1 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
+
+
+def capture(torch, fn, n):
+    """A CUDA graph of fn(0) .. fn(n-1).  fn is called once beforehand (outside
+    the capture) so one-time library set-up does not happen while capturing."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn(0)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(torch, g, replays):
+    """ms for `replays` back-to-back replays, CUDA events on the launching stream."""
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(replays):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
 
 
 def load_traffic(key):
@@ -267,7 +299,8 @@ def load_traffic(key):
 
 
 def bench_layers(qm, synth, dev, stream, args):
-    """MoE decode (us/token), dense FFN (us/call), MoE 512-token layer (us/token)."""
+    """MoE decode (us/token), dense FFN (us/call), MoE 512-token layer
+    (us/token); each captured in a CUDA graph and replayed."""
     import torch
     out = {}
     peak, _ = load_peaks()
@@ -286,18 +319,12 @@ def bench_layers(qm, synth, dev, stream, args):
 
     def call(i):
         qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, xpool[i % 64], res, idx, None,
-                   ws, stream=stream)
-    for i in range(10):
-        call(i)
-    torch.cuda.synchronize()
-    n = 200
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(n):
-        call(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / n
+                   ws)
+    n = 64
+    gm = capture(torch, call, n)
+    gm.replay()
+    reps = 4
+    us = time_replays(torch, gm, reps) * 1e3 / (reps * n)
     rb_g = qm.row_bytes(shp["gate"], shp["hidden"])
     rb_d = qm.row_bytes(shp["down"], shp["expert_dim"])
     alg = (shp["num_experts"] * shp["hidden"] * 4
@@ -305,9 +332,9 @@ def bench_layers(qm, synth, dev, stream, args):
            + 3 * shp["hidden"] * 4)
     out["moe_decode"] = {"us_per_token": round(us, 3), "alg_bytes": alg,
                          "gbs": round(alg / us / 1e3, 1), "frac": round(alg / us / 1e3 / peak, 3),
-                         "launches_per_token": 3,
+                         "launches_per_token": 3, "launch": f"CUDA graph of {n} tokens",
                          "workload": "hidden 2048, 128 experts, top-8, expert_dim 768, Q4_K/Q4_K/Q6_K"}
-    del d, inp
+    del d, inp, gm
     torch.cuda.empty_cache()
 
     # dense SwiGLU FFN: 114 MB weights, 5 copies rotating (> 4x L2)
@@ -325,22 +352,17 @@ def bench_layers(qm, synth, dev, stream, args):
     def fcall(i):
         c = i % ncp
         qm.ffn_swiglu(G[c], U[c], D[c], w["gate"], w["up"], w["down"], w["hidden"], w["inter"],
-                      x, r, ws, stream=stream)
-    for i in range(5):
-        fcall(i)
-    torch.cuda.synchronize()
-    n = 40
-    e0.record(stream)
-    for i in range(n):
-        fcall(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / n
+                      x, r, ws)
+    n = 2 * ncp
+    gf = capture(torch, fcall, n)
+    gf.replay()
+    us = time_replays(torch, gf, 4) * 1e3 / (4 * n)
     alg = fin["gate"].nbytes + fin["up"].nbytes + fin["down"].nbytes + 4 * w["hidden"] * 3
     out["dense_ffn"] = {"us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1),
-                        "frac": round(alg / us / 1e3 / peak, 3),
+                        "frac": round(alg / us / 1e3 / peak, 3), "launches": 2,
+                        "launch": f"CUDA graph of {n} calls",
                         "workload": "hidden 4096, intermediate 14336, Q4_K/Q4_K/Q6_K"}
-    del G, U, D
+    del G, U, D, gf
     torch.cuda.empty_cache()
 
     # MoE 512-token layer
@@ -352,20 +374,24 @@ def bench_layers(qm, synth, dev, stream, args):
                                                           "residual")}
     ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device=dev)
 
-    def pcall():
+    def pcall(i):
         qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, d["x"], d["residual"], None,
-                   None, ws, stream=stream)
-    pcall()
-    torch.cuda.synchronize()
+                   None, ws)
+    gp = capture(torch, pcall, 1)
+    gp.replay()
     n = 3
-    e0.record(stream)
-    for _ in range(n):
-        pcall()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / n
+    us = time_replays(torch, gp, n) * 1e3 / n
+    rb_g = qm.row_bytes(shp["gate"], shp["hidden"])
+    rb_d = qm.row_bytes(shp["down"], shp["expert_dim"])
+    alg_w = shp["num_experts"] * (2 * shp["expert_dim"] * rb_g + shp["hidden"] * rb_d)
+    alg = alg_w + shp["num_experts"] * shp["hidden"] * 4 + 3 * shp["n_tokens"] * shp["hidden"] * 4
+    flops = 2 * shp["n_tokens"] * shp["top_k"] * 3 * shp["hidden"] * shp["expert_dim"]
     out["moe_prefill"] = {"us_per_call": round(us, 1),
                           "us_per_token": round(us / shp["n_tokens"], 3),
+                          "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1),
+                          "frac_hbm": round(alg / us / 1e3 / peak, 4),
+                          "expert_tflops": round(flops / us / 1e6, 2),
+                          "launch": "CUDA graph of one call",
                           "workload": "512 tokens, hidden 2048, 64 experts, top-8, "
                                       "expert_dim 1024, Q4_K/Q4_K/Q6_K"}
     return out
@@ -441,7 +467,7 @@ def run_reference(args, rank, world):
 
 def run_profile_case(case, launches):
     """Minimal program for ncu: one workload, `launches` calls, nothing else.
-    gemv:<FMT> — one 4096x4096 GEMV of that format; moe — the decode layer;
+    gemv:<FMT>[:rows] — one [rows]x4096 GEMV (default 4096 rows); moe — the decode layer;
     ffn — the dense FFN."""
     import torch
 
@@ -450,14 +476,16 @@ def run_profile_case(case, launches):
     qm.build()
     dev = torch.device("cuda", 0)
     if case.startswith("gemv:"):
-        name = case.split(":", 1)[1]
+        parts = case.split(":")
+        name = parts[1]
+        rows = int(parts[2]) if len(parts) > 2 else ROWS
         qt = dict(FORMATS)[name]
         g = synth.rng(qt)
-        W = torch.from_numpy(synth.quant_matrix(g, qt, ROWS, COLS, nan_row=1)).to(dev)
+        W = torch.from_numpy(synth.quant_matrix(g, qt, rows, COLS, nan_row=1)).to(dev)
         x = torch.from_numpy(synth.normal(g, COLS)).to(dev)
-        y = torch.empty(ROWS, device=dev)
+        y = torch.empty(rows, device=dev)
         for _ in range(launches):
-            qm.qmv(qt, W, ROWS, COLS, x, y)
+            qm.qmv(qt, W, rows, COLS, x, y)
     elif case == "moe":
         shp = synth.MOE_DECODE
         inp = synth.moe_inputs(0, **shp)

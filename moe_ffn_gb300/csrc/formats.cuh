@@ -23,7 +23,9 @@
 // Q8_0/Q4_0, 8 consecutive 32-element blocks).  It processes 64 elements;
 // element i (0..63) of its quarter is elem(q,i) of the group, and sits at
 // bit offset pos(q,i) after extraction.  x' is stored in shared memory as
-// float4 [group][i/4][q] so the four quarter-lanes read 64 contiguous bytes.
+// float4 [group][i/4][q] so the four quarter-lanes read 64 contiguous bytes;
+// a lane loads its 64 values into registers once (load_xq) and applies them
+// to several rows (dot).
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -41,6 +43,13 @@ __device__ __forceinline__ float qfma(uint32_t masked_bits, float xs, float acc)
     return fmaf(__uint_as_float(masked_bits), xs, acc);
 }
 
+// Two fields at once on the packed f32x2 FMA: acc.{x,y} += q{0,1} * x{0,1}.
+__device__ __forceinline__ float2 qfma2(uint32_t m0, uint32_t m1, float x0, float x1,
+                                        float2 acc) {
+    return __ffma2_rn(make_float2(__uint_as_float(m0), __uint_as_float(m1)),
+                      make_float2(x0, x1), acc);
+}
+
 // 2^(85 - pos) as a float, exact.
 __host__ __device__ __forceinline__ float xprime_scale(int pos) {
 #ifdef __CUDA_ARCH__
@@ -55,6 +64,25 @@ __host__ __device__ __forceinline__ float xprime_scale(int pos) {
 // 2^64, folded into d.
 constexpr float TWO64 = 18446744073709551616.0f;
 
+// Bits [24, 24+n) of w isolated at bit 0, on the multiply pipe:
+// (w << (8-n)) keeps them topmost, the high half of * 2^n keeps only them.
+template <int N>
+__device__ __forceinline__ uint32_t top_field(uint32_t w) {
+    return __umulhi(w << (8 - N), 1u << N);
+}
+
+// The 64 x' values of quarter q of one group, from the interleaved table.
+__device__ __forceinline__ void load_xq(const float4* xq_group, int q, float (&x)[64]) {
+#pragma unroll
+    for (int i4 = 0; i4 < 16; ++i4) {
+        const float4 v = xq_group[i4 * 4 + q];
+        x[4 * i4] = v.x;
+        x[4 * i4 + 1] = v.y;
+        x[4 * i4 + 2] = v.z;
+        x[4 * i4 + 3] = v.w;
+    }
+}
+
 // Read 4 consecutive 32-bit words starting at a 2-byte-aligned shared-memory
 // address: aligned loads plus a funnel shift by 0 or 16 bits.
 __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) {
@@ -68,6 +96,14 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
     for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(r[k], r[k + 1], sh);
 }
 
+// Every format provides
+//   elem(q, i), pos(q, i)  — the lane element order and extraction offsets;
+//   dotR<R>(sb[R], q, x, xs16, acc[R]) — for R rows whose super-blocks start
+//   at sb[r] (shared memory), adds each row's dot over the lane's quarter to
+//   acc[r].  Words of all R rows are loaded first and the element loop runs
+//   over words with the rows innermost, so a lane carries 4R independent
+//   FFMA chains.
+
 // ------------------------------------------------------------------ Q4_K
 // 144-byte super-block: f16 d @0, f16 dmin @2, 12 bytes of 6-bit (sc, m)
 // pairs @4, qs[128] @16.  Quarter q = group oi of the page kernel: qs bytes
@@ -77,8 +113,8 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
 // Lane element order: word t (bytes 4t..4t+3), i = 8t + j: j<4 -> low
 // nibble of byte j, j>=4 -> high nibble of byte j-4.
 // Extraction per word W: lo b0 &0xF (0), lo b1 &0xF00 (8), lo b2 &0xF0000
-// (16), hi b0 &0xF0 (4), hi b1 &0xF000 (12), hi b2 &0xF00000 (20); byte 3
-// via W>>24: lo &0xF (0), hi &0xF0 (4).
+// (16), hi b0 &0xF0 (4), hi b1 &0xF000 (12), hi b2 &0xF00000 (20); byte 3's
+// nibbles come from the multiply pipe (top_field, __umulhi): both at bit 0.
 struct FmtQ4K {
     static constexpr int SBB = 144;
     __host__ __device__ static int elem(int q, int i) {
@@ -86,60 +122,68 @@ struct FmtQ4K {
         return j < 4 ? 64 * q + 4 * t + j : 64 * q + 32 + 4 * t + (j - 4);
     }
     __host__ __device__ static int pos(int, int i) {
-        // bit offsets {0, 8, 16, 0, 4, 12, 20, 4} by i % 8, one byte each
-        return static_cast<int>((0x04140C0400100800ull >> (8 * (i & 7))) & 0xFFu);
+        // bit offsets {0, 8, 16, 0, 4, 12, 20, 0} by i % 8, one byte each
+        return static_cast<int>((0x00140C0400100800ull >> (8 * (i & 7))) & 0xFFu);
     }
     // 6-bit (sc, m) of pairs 2q and 2q+1 — the unpacking of
-    // ferrox_q4_k_scale_min, written branch-free over the lane's q.
+    // ferrox_q4_k_scale_min, four pairs per 32-bit word: pairs 0..3 are the
+    // low 6 bits of bytes 0..3 (sc) and 4..7 (m); pairs 4..7 join the low /
+    // high nibble of bytes 8..11 with the top two bits of bytes 0..3 / 4..7.
+    // The lane's word is selected branch-free; bytes become floats on the
+    // conversion pipe.
     __device__ __forceinline__ static void scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int q,
                                                      float& sca, float& ma, float& scb,
                                                      float& mb) {
-        const bool hi = q >= 2;               // pairs j >= 4
-        const int b = (2 * q) & 3;            // byte of pair 2q within its word
-        const uint32_t lsc = hi ? s2 : s0;    // low nibble source for sc
-        const uint32_t lm = hi ? s2 : s1;     // low nibble source for m
-        const int lsc_sh = 8 * b, lm_sh = hi ? 8 * b + 4 : 8 * b;
-        const int hsh = hi ? 8 * b + 6 : 8 * b + 4;
-        // pair 2q (byte b) and 2q+1 (byte b+1)
-        uint32_t sc0 = ((lsc >> lsc_sh) & 15u) | (((s0 >> hsh) & 3u) << 4);
-        uint32_t m0 = ((lm >> lm_sh) & 15u) | (((s1 >> hsh) & 3u) << 4);
-        uint32_t sc1 = ((lsc >> (lsc_sh + 8)) & 15u) | (((s0 >> (hsh + 8)) & 3u) << 4);
-        uint32_t m1 = ((lm >> (lm_sh + 8)) & 15u) | (((s1 >> (hsh + 8)) & 3u) << 4);
-        sca = static_cast<float>(sc0);
-        ma = static_cast<float>(m0);
-        scb = static_cast<float>(sc1);
-        mb = static_cast<float>(m1);
+        const bool hi = q >= 2;
+        const uint32_t sc_w =
+            ((hi ? s2 : s0) & 0x0F0F0F0Fu) | ((hi ? (s0 >> 2) : s0) & 0x30303030u);
+        const uint32_t m_w =
+            ((hi ? (s2 >> 4) : s1) & 0x0F0F0F0Fu) | ((hi ? (s1 >> 2) : s1) & 0x30303030u);
+        const int sh = 16 * (q & 1);  // pairs 2q, 2q+1 are bytes 2(q&1), 2(q&1)+1
+        sca = static_cast<float>((sc_w >> sh) & 0xFFu);
+        scb = static_cast<float>((sc_w >> (sh + 8)) & 0xFFu);
+        ma = static_cast<float>((m_w >> sh) & 0xFFu);
+        mb = static_cast<float>((m_w >> (sh + 8)) & 0xFFu);
     }
-    __device__ __forceinline__ static float dot(const uint8_t* sb, int q, const float4* xq,
-                                                const float* xs16) {
-        const uint4 h = *reinterpret_cast<const uint4*>(sb);
-        const float d = f16_bits_to_f32(h.x) * TWO64;
-        const float dmin = f16_bits_to_f32(h.x >> 16);
-        float sca, ma, scb, mb;
-        scale_min(h.y, h.z, h.w, q, sca, ma, scb, mb);
-        const uint4 wa = *reinterpret_cast<const uint4*>(sb + 16 + 32 * q);
-        const uint4 wb = *reinterpret_cast<const uint4*>(sb + 16 + 32 * q + 16);
-        const uint32_t W[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-        float alo = 0.f, ahi = 0.f, alo2 = 0.f, ahi2 = 0.f;
+    template <int R>
+    __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
+                                                const float (&x)[64], const float* xs16,
+                                                float (&acc)[R]) {
+        uint32_t W[R][8];
+        uint4 h[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            h[r] = *reinterpret_cast<const uint4*>(sb[r]);
+            const uint4 wa = *reinterpret_cast<const uint4*>(sb[r] + 16 + 32 * q);
+            const uint4 wb = *reinterpret_cast<const uint4*>(sb[r] + 16 + 32 * q + 16);
+            W[r][0] = wa.x; W[r][1] = wa.y; W[r][2] = wa.z; W[r][3] = wa.w;
+            W[r][4] = wb.x; W[r][5] = wb.y; W[r][6] = wb.z; W[r][7] = wb.w;
+        }
+        float2 alo[R], ahi[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) alo[r] = ahi[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const uint32_t w = W[t], v = w >> 24;
-            const float4 xl = xq[(2 * t) * 4 + q];
-            const float4 xh = xq[(2 * t + 1) * 4 + q];
-            alo = qfma(w & 0xFu, xl.x, alo);
-            alo2 = qfma(w & 0xF00u, xl.y, alo2);
-            alo = qfma(w & 0xF0000u, xl.z, alo);
-            alo2 = qfma(v & 0xFu, xl.w, alo2);
-            ahi = qfma(w & 0xF0u, xh.x, ahi);
-            ahi2 = qfma(w & 0xF000u, xh.y, ahi2);
-            ahi = qfma(w & 0xF00000u, xh.z, ahi);
-            ahi2 = qfma(v & 0xF0u, xh.w, ahi2);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t w = W[r][t];
+                alo[r] = qfma2(w & 0xFu, w & 0xF00u, x[8 * t], x[8 * t + 1], alo[r]);
+                alo[r] = qfma2(w & 0xF0000u, top_field<4>(w), x[8 * t + 2], x[8 * t + 3], alo[r]);
+                ahi[r] = qfma2(w & 0xF0u, w & 0xF000u, x[8 * t + 4], x[8 * t + 5], ahi[r]);
+                ahi[r] = qfma2(w & 0xF00000u, __umulhi(w, 16u), x[8 * t + 6], x[8 * t + 7], ahi[r]);
+            }
         }
-        alo += alo2;
-        ahi += ahi2;
         const float Xa = xs16[4 * q] + xs16[4 * q + 1];
         const float Xb = xs16[4 * q + 2] + xs16[4 * q + 3];
-        return d * fmaf(sca, alo, scb * ahi) - dmin * fmaf(ma, Xa, mb * Xb);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float sca, ma, scb, mb;
+            scale_min(h[r].y, h[r].z, h[r].w, q, sca, ma, scb, mb);
+            const float d = f16_bits_to_f32(h[r].x) * TWO64;
+            const float dmin = f16_bits_to_f32(h[r].x >> 16);
+            acc[r] += d * fmaf(sca, alo[r].x + alo[r].y, scb * (ahi[r].x + ahi[r].y)) -
+                      dmin * fmaf(ma, Xa, mb * Xb);
+        }
     }
 };
 
@@ -148,53 +192,64 @@ struct FmtQ4K {
 // As Q4_K, plus 16 where bit 2q (low half) / 2q+1 (high half) of qh[l] is
 // set.  The qh bit is rotated into bit 4 of each byte and merged with the
 // nibble (bits 5..7 of the merge are don't-care: the 5-bit mask drops them).
-// Lane element order as Q4_K; positions: byte k -> 8k for k<3, byte 3 via
-// >>8 -> 16.
+// Lane element order as Q4_K; positions: byte k -> 8k for k<3, byte 3's
+// field from the multiply pipe -> 0.
 struct FmtQ5K {
     static constexpr int SBB = 176;
     __host__ __device__ static int elem(int q, int i) { return FmtQ4K::elem(q, i); }
     __host__ __device__ static int pos(int, int i) {
-        // bit offsets {0, 8, 16, 16} by i % 4
-        return static_cast<int>((0x10100800u >> (8 * (i & 3))) & 0xFFu);
+        // bit offsets {0, 8, 16, 0} by i % 4
+        return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
     }
-    __device__ __forceinline__ static float dot(const uint8_t* sb, int q, const float4* xq,
-                                                const float* xs16) {
-        const uint4 h = *reinterpret_cast<const uint4*>(sb);
-        const float d = f16_bits_to_f32(h.x) * TWO64;
-        const float dmin = f16_bits_to_f32(h.x >> 16);
-        float sca, ma, scb, mb;
-        FmtQ4K::scale_min(h.y, h.z, h.w, q, sca, ma, scb, mb);
-        const uint4 qa = *reinterpret_cast<const uint4*>(sb + 48 + 32 * q);
-        const uint4 qb = *reinterpret_cast<const uint4*>(sb + 48 + 32 * q + 16);
-        const uint4 ha = *reinterpret_cast<const uint4*>(sb + 16);
-        const uint4 hb = *reinterpret_cast<const uint4*>(sb + 32);
-        const uint32_t W[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-        const uint32_t H[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+    template <int R>
+    __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
+                                                const float (&x)[64], const float* xs16,
+                                                float (&acc)[R]) {
         const uint32_t rlo = static_cast<uint32_t>(4 - 2 * q) & 31u;
         const uint32_t rhi = static_cast<uint32_t>(3 - 2 * q) & 31u;
-        float alo = 0.f, ahi = 0.f, alo2 = 0.f, ahi2 = 0.f;
+        uint32_t W[R][8], H[R][8];
+        uint4 h[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            h[r] = *reinterpret_cast<const uint4*>(sb[r]);
+            const uint4 qa = *reinterpret_cast<const uint4*>(sb[r] + 48 + 32 * q);
+            const uint4 qb = *reinterpret_cast<const uint4*>(sb[r] + 48 + 32 * q + 16);
+            const uint4 ha = *reinterpret_cast<const uint4*>(sb[r] + 16);
+            const uint4 hb = *reinterpret_cast<const uint4*>(sb[r] + 32);
+            W[r][0] = qa.x; W[r][1] = qa.y; W[r][2] = qa.z; W[r][3] = qa.w;
+            W[r][4] = qb.x; W[r][5] = qb.y; W[r][6] = qb.z; W[r][7] = qb.w;
+            H[r][0] = ha.x; H[r][1] = ha.y; H[r][2] = ha.z; H[r][3] = ha.w;
+            H[r][4] = hb.x; H[r][5] = hb.y; H[r][6] = hb.z; H[r][7] = hb.w;
+        }
+        float2 alo[R], ahi[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) alo[r] = ahi[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const uint32_t w = W[t], hw = H[t];
-            const uint32_t lo = (w & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rlo) & 0xF0F0F0F0u);
-            const uint32_t hi =
-                ((w >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rhi) & 0xF0F0F0F0u);
-            const float4 xl = xq[(2 * t) * 4 + q];
-            const float4 xh = xq[(2 * t + 1) * 4 + q];
-            alo = qfma(lo & 0x1Fu, xl.x, alo);
-            alo2 = qfma(lo & 0x1F00u, xl.y, alo2);
-            alo = qfma(lo & 0x1F0000u, xl.z, alo);
-            alo2 = qfma((lo >> 8) & 0x1F0000u, xl.w, alo2);
-            ahi = qfma(hi & 0x1Fu, xh.x, ahi);
-            ahi2 = qfma(hi & 0x1F00u, xh.y, ahi2);
-            ahi = qfma(hi & 0x1F0000u, xh.z, ahi);
-            ahi2 = qfma((hi >> 8) & 0x1F0000u, xh.w, ahi2);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t w = W[r][t], hw = H[r][t];
+                const uint32_t lo =
+                    (w & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rlo) & 0xF0F0F0F0u);
+                const uint32_t hi =
+                    ((w >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rhi) & 0xF0F0F0F0u);
+                alo[r] = qfma2(lo & 0x1Fu, lo & 0x1F00u, x[8 * t], x[8 * t + 1], alo[r]);
+                alo[r] = qfma2(lo & 0x1F0000u, top_field<5>(lo), x[8 * t + 2], x[8 * t + 3], alo[r]);
+                ahi[r] = qfma2(hi & 0x1Fu, hi & 0x1F00u, x[8 * t + 4], x[8 * t + 5], ahi[r]);
+                ahi[r] = qfma2(hi & 0x1F0000u, top_field<5>(hi), x[8 * t + 6], x[8 * t + 7], ahi[r]);
+            }
         }
-        alo += alo2;
-        ahi += ahi2;
         const float Xa = xs16[4 * q] + xs16[4 * q + 1];
         const float Xb = xs16[4 * q + 2] + xs16[4 * q + 3];
-        return d * fmaf(sca, alo, scb * ahi) - dmin * fmaf(ma, Xa, mb * Xb);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float sca, ma, scb, mb;
+            FmtQ4K::scale_min(h[r].y, h[r].z, h[r].w, q, sca, ma, scb, mb);
+            const float d = f16_bits_to_f32(h[r].x) * TWO64;
+            const float dmin = f16_bits_to_f32(h[r].x >> 16);
+            acc[r] += d * fmaf(sca, alo[r].x + alo[r].y, scb * (ahi[r].x + ahi[r].y)) -
+                      dmin * fmaf(ma, Xa, mb * Xb);
+        }
     }
 };
 
@@ -206,7 +261,7 @@ struct FmtQ5K {
 // sc[8h + c + {0,2,4,6}]; value (d*sc)*(q-32).  Super-blocks are only
 // 2-byte aligned, so words are read with funnel shifts.
 // Lane element order: i = 16u + 4t + j -> element 128h + 32t + 16c + 4u + j;
-// positions (0, 8, 16, 16).
+// positions (0, 8, 16, 0) (byte 3's field from the multiply pipe).
 struct FmtQ6K {
     static constexpr int SBB = 210;
     __host__ __device__ static int elem(int q, int i) {
@@ -214,63 +269,67 @@ struct FmtQ6K {
         return 128 * (q >> 1) + 32 * t + 16 * (q & 1) + 4 * u + j;
     }
     __host__ __device__ static int pos(int, int i) {
-        // bit offsets {0, 8, 16, 16} by i % 4
-        return static_cast<int>((0x10100800u >> (8 * (i & 3))) & 0xFFu);
+        // bit offsets {0, 8, 16, 0} by i % 4
+        return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
     }
-    __device__ __forceinline__ static float dot(const uint8_t* sb, int q, const float4* xq,
-                                                const float* xs16) {
+    template <int R>
+    __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
+                                                const float (&x)[64], const float* xs16,
+                                                float (&acc)[R]) {
         const int h = q >> 1, c = q & 1;
-        uint32_t A[4], B[4], H[4], S[4];
-        load4_u16al(sb + 64 * h + 16 * c, A);
-        load4_u16al(sb + 64 * h + 32 + 16 * c, B);
-        load4_u16al(sb + 128 + 32 * h + 16 * c, H);
-        load4_u16al(sb + 192, S);  // S[0..3] = sc[0..15]; S[4] would overrun: d read below
-        const uintptr_t a = reinterpret_cast<uintptr_t>(sb + 208);
-        const uint32_t dw = *reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-        const float d = f16_bits_to_f32(dw >> ((a & 3u) * 8u));
-        const float d64 = d * TWO64, d32 = -32.f * d;
-        // scales sc[8h + c + 2t], t = 0..3: bytes of S[2h], S[2h+1]
-        const uint32_t s_lo = S[2 * h], s_hi = S[2 * h + 1];
-        const float sc0 = static_cast<float>(static_cast<int8_t>(s_lo >> (8 * c)));
-        const float sc1 = static_cast<float>(static_cast<int8_t>(s_lo >> (8 * c + 16)));
-        const float sc2 = static_cast<float>(static_cast<int8_t>(s_hi >> (8 * c)));
-        const float sc3 = static_cast<float>(static_cast<int8_t>(s_hi >> (8 * c + 16)));
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        uint32_t A[R][4], B[R][4], H[R][4];
+        float sc[R][4], d[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            load4_u16al(sb[r] + 64 * h + 16 * c, A[r]);
+            load4_u16al(sb[r] + 64 * h + 32 + 16 * c, B[r]);
+            load4_u16al(sb[r] + 128 + 32 * h + 16 * c, H[r]);
+            uint32_t S[4];
+            load4_u16al(sb[r] + 192, S);  // sc[0..15]
+            const uintptr_t a = reinterpret_cast<uintptr_t>(sb[r] + 208);
+            const uint32_t dw = *reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+            d[r] = f16_bits_to_f32(dw >> ((a & 3u) * 8u));
+            // scales sc[8h + c + 2t], t = 0..3: bytes of S[2h], S[2h+1]
+            const uint32_t s_lo = S[2 * h], s_hi = S[2 * h + 1];
+            sc[r][0] = static_cast<float>(static_cast<int8_t>(s_lo >> (8 * c)));
+            sc[r][1] = static_cast<float>(static_cast<int8_t>(s_lo >> (8 * c + 16)));
+            sc[r][2] = static_cast<float>(static_cast<int8_t>(s_hi >> (8 * c)));
+            sc[r][3] = static_cast<float>(static_cast<int8_t>(s_hi >> (8 * c + 16)));
+        }
+        float2 a0[R], a1[R], a2[R], a3[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) a0[r] = a1[r] = a2[r] = a3[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const uint32_t av = A[u], bv = B[u], hv = H[u];
-            const uint32_t v0 = (av & 0x0F0F0F0Fu) | ((hv << 4) & 0xF0F0F0F0u);
-            const uint32_t v1 = (bv & 0x0F0F0F0Fu) | ((hv << 2) & 0xF0F0F0F0u);
-            const uint32_t v2 = ((av >> 4) & 0x0F0F0F0Fu) | (hv & 0xF0F0F0F0u);
-            const uint32_t v3 = ((bv >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0xF0F0F0F0u);
-            const float4 x0 = xq[(4 * u + 0) * 4 + q];
-            const float4 x1 = xq[(4 * u + 1) * 4 + q];
-            const float4 x2 = xq[(4 * u + 2) * 4 + q];
-            const float4 x3 = xq[(4 * u + 3) * 4 + q];
-            a0 = qfma(v0 & 0x3Fu, x0.x, a0);
-            a0 = qfma(v0 & 0x3F00u, x0.y, a0);
-            a0 = qfma(v0 & 0x3F0000u, x0.z, a0);
-            a0 = qfma((v0 >> 8) & 0x3F0000u, x0.w, a0);
-            a1 = qfma(v1 & 0x3Fu, x1.x, a1);
-            a1 = qfma(v1 & 0x3F00u, x1.y, a1);
-            a1 = qfma(v1 & 0x3F0000u, x1.z, a1);
-            a1 = qfma((v1 >> 8) & 0x3F0000u, x1.w, a1);
-            a2 = qfma(v2 & 0x3Fu, x2.x, a2);
-            a2 = qfma(v2 & 0x3F00u, x2.y, a2);
-            a2 = qfma(v2 & 0x3F0000u, x2.z, a2);
-            a2 = qfma((v2 >> 8) & 0x3F0000u, x2.w, a2);
-            a3 = qfma(v3 & 0x3Fu, x3.x, a3);
-            a3 = qfma(v3 & 0x3F00u, x3.y, a3);
-            a3 = qfma(v3 & 0x3F0000u, x3.z, a3);
-            a3 = qfma((v3 >> 8) & 0x3F0000u, x3.w, a3);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t av = A[r][u], bv = B[r][u], hv = H[r][u];
+                const uint32_t v0 = (av & 0x0F0F0F0Fu) | ((hv << 4) & 0xF0F0F0F0u);
+                const uint32_t v1 = (bv & 0x0F0F0F0Fu) | ((hv << 2) & 0xF0F0F0F0u);
+                const uint32_t v2 = ((av >> 4) & 0x0F0F0F0Fu) | (hv & 0xF0F0F0F0u);
+                const uint32_t v3 = ((bv >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0xF0F0F0F0u);
+                const float* xu = x + 16 * u;
+                a0[r] = qfma2(v0 & 0x3Fu, v0 & 0x3F00u, xu[0], xu[1], a0[r]);
+                a0[r] = qfma2(v0 & 0x3F0000u, top_field<6>(v0), xu[2], xu[3], a0[r]);
+                a1[r] = qfma2(v1 & 0x3Fu, v1 & 0x3F00u, xu[4], xu[5], a1[r]);
+                a1[r] = qfma2(v1 & 0x3F0000u, top_field<6>(v1), xu[6], xu[7], a1[r]);
+                a2[r] = qfma2(v2 & 0x3Fu, v2 & 0x3F00u, xu[8], xu[9], a2[r]);
+                a2[r] = qfma2(v2 & 0x3F0000u, top_field<6>(v2), xu[10], xu[11], a2[r]);
+                a3[r] = qfma2(v3 & 0x3Fu, v3 & 0x3F00u, xu[12], xu[13], a3[r]);
+                a3[r] = qfma2(v3 & 0x3F0000u, top_field<6>(v3), xu[14], xu[15], a3[r]);
+            }
         }
         // 16-element groups of this lane: 8h + 2t + c
         const float* X = xs16 + 8 * h + c;
-        float r = sc0 * fmaf(d32, X[0], a0 * d64);
-        r = fmaf(sc1, fmaf(d32, X[2], a1 * d64), r);
-        r = fmaf(sc2, fmaf(d32, X[4], a2 * d64), r);
-        r = fmaf(sc3, fmaf(d32, X[6], a3 * d64), r);
-        return r;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float d64 = d[r] * TWO64, d32 = -32.f * d[r];
+            float res = sc[r][0] * fmaf(d32, X[0], (a0[r].x + a0[r].y) * d64);
+            res = fmaf(sc[r][1], fmaf(d32, X[2], (a1[r].x + a1[r].y) * d64), res);
+            res = fmaf(sc[r][2], fmaf(d32, X[4], (a2[r].x + a2[r].y) * d64), res);
+            res = fmaf(sc[r][3], fmaf(d32, X[6], (a3[r].x + a3[r].y) * d64), res);
+            acc[r] += res;
+        }
     }
 };
 
@@ -288,35 +347,45 @@ struct FmtQ80 {
         // bit offsets {0, 8, 16, 0} by i % 4
         return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
     }
-    __device__ __forceinline__ static float dot(const uint8_t* sb, int q, const float4* xq,
-                                                const float* xs16) {
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(sb + 68 * q);
-        uint32_t U[17];
+    template <int R>
+    __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
+                                                const float (&x)[64], const float* xs16,
+                                                float (&acc)[R]) {
+        uint32_t U[R][17];
 #pragma unroll
-        for (int k = 0; k < 17; ++k) U[k] = u[k];
-        const float dA = f16_bits_to_f32(U[0]);
-        const float dB = f16_bits_to_f32(U[8] >> 16);
-        float aA = 0.f, aB = 0.f, aA2 = 0.f, aB2 = 0.f;
+        for (int r = 0; r < R; ++r) {
+            const uint32_t* u = reinterpret_cast<const uint32_t*>(sb[r] + 68 * q);
+#pragma unroll
+            for (int k = 0; k < 17; ++k) U[r][k] = u[k];
+        }
+        float2 aA[R], aB[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) aA[r] = aB[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const uint32_t wa = __funnelshift_r(U[t], U[t + 1], 16) ^ 0x80808080u;
-            const uint32_t wb = U[9 + t] ^ 0x80808080u;
-            const float4 xa = xq[t * 4 + q];
-            const float4 xb = xq[(8 + t) * 4 + q];
-            aA = qfma(wa & 0xFFu, xa.x, aA);
-            aA2 = qfma(wa & 0xFF00u, xa.y, aA2);
-            aA = qfma(wa & 0xFF0000u, xa.z, aA);
-            aA2 = qfma(wa >> 24, xa.w, aA2);
-            aB = qfma(wb & 0xFFu, xb.x, aB);
-            aB2 = qfma(wb & 0xFF00u, xb.y, aB2);
-            aB = qfma(wb & 0xFF0000u, xb.z, aB);
-            aB2 = qfma(wb >> 24, xb.w, aB2);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t wa = __funnelshift_r(U[r][t], U[r][t + 1], 16);
+                const uint32_t wb = U[r][9 + t];
+                aA[r] = qfma2((wa ^ 0x80808080u) & 0xFFu, (wa ^ 0x80808080u) & 0xFF00u, x[4 * t],
+                              x[4 * t + 1], aA[r]);
+                aA[r] = qfma2((wa ^ 0x80808080u) & 0xFF0000u, __umulhi(wa + 0x80000000u, 256u),
+                              x[4 * t + 2], x[4 * t + 3], aA[r]);
+                aB[r] = qfma2((wb ^ 0x80808080u) & 0xFFu, (wb ^ 0x80808080u) & 0xFF00u,
+                              x[32 + 4 * t], x[33 + 4 * t], aB[r]);
+                aB[r] = qfma2((wb ^ 0x80808080u) & 0xFF0000u, __umulhi(wb + 0x80000000u, 256u),
+                              x[34 + 4 * t], x[35 + 4 * t], aB[r]);
+            }
         }
-        aA += aA2;
-        aB += aB2;
         const float XA = xs16[4 * q] + xs16[4 * q + 1];
         const float XB = xs16[4 * q + 2] + xs16[4 * q + 3];
-        return dA * fmaf(aA, TWO64, -128.f * XA) + dB * fmaf(aB, TWO64, -128.f * XB);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float dA = f16_bits_to_f32(U[r][0]);
+            const float dB = f16_bits_to_f32(U[r][8] >> 16);
+            acc[r] += dA * fmaf(aA[r].x + aA[r].y, TWO64, -128.f * XA) +
+                      dB * fmaf(aB[r].x + aB[r].y, TWO64, -128.f * XB);
+        }
     }
 };
 
@@ -334,40 +403,45 @@ struct FmtQ40 {
         return j < 4 ? base + 4 * t + j : base + 16 + 4 * t + (j - 4);
     }
     __host__ __device__ static int pos(int q, int i) { return FmtQ4K::pos(q, i); }
-    __device__ __forceinline__ static float dot(const uint8_t* sb, int q, const float4* xq,
-                                                const float* xs16) {
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(sb + 36 * q);
-        uint32_t U[9];
+    template <int R>
+    __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
+                                                const float (&x)[64], const float* xs16,
+                                                float (&acc)[R]) {
+        uint32_t U[R][9];
 #pragma unroll
-        for (int k = 0; k < 9; ++k) U[k] = u[k];
-        const float dA = f16_bits_to_f32(U[0]);
-        const float dB = f16_bits_to_f32(U[4] >> 16);
-        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        for (int r = 0; r < R; ++r) {
+            const uint32_t* u = reinterpret_cast<const uint32_t*>(sb[r] + 36 * q);
+#pragma unroll
+            for (int k = 0; k < 9; ++k) U[r][k] = u[k];
+        }
+        float2 a[R][2];
+#pragma unroll
+        for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const uint32_t w = k == 0 ? __funnelshift_r(U[t], U[t + 1], 16) : U[5 + t];
-                const uint32_t v = w >> 24;
-                const float4 xl = xq[(8 * k + 2 * t) * 4 + q];
-                const float4 xh = xq[(8 * k + 2 * t + 1) * 4 + q];
-                float a = acc[k][0], b = acc[k][1];
-                a = qfma(w & 0xFu, xl.x, a);
-                b = qfma(w & 0xF00u, xl.y, b);
-                a = qfma(w & 0xF0000u, xl.z, a);
-                b = qfma(v & 0xFu, xl.w, b);
-                a = qfma(w & 0xF0u, xh.x, a);
-                b = qfma(w & 0xF000u, xh.y, b);
-                a = qfma(w & 0xF00000u, xh.z, a);
-                b = qfma(v & 0xF0u, xh.w, b);
-                acc[k][0] = a;
-                acc[k][1] = b;
+                const int o = 32 * k + 8 * t;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t w = k == 0 ? __funnelshift_r(U[r][t], U[r][t + 1], 16)
+                                              : U[r][5 + t];
+                    a[r][k] = qfma2(w & 0xFu, w & 0xF00u, x[o], x[o + 1], a[r][k]);
+                    a[r][k] = qfma2(w & 0xF0000u, top_field<4>(w), x[o + 2], x[o + 3], a[r][k]);
+                    a[r][k] = qfma2(w & 0xF0u, w & 0xF000u, x[o + 4], x[o + 5], a[r][k]);
+                    a[r][k] = qfma2(w & 0xF00000u, __umulhi(w, 16u), x[o + 6], x[o + 7], a[r][k]);
+                }
             }
         }
-        const float aA = acc[0][0] + acc[0][1], aB = acc[1][0] + acc[1][1];
         const float XA = xs16[4 * q] + xs16[4 * q + 1];
         const float XB = xs16[4 * q + 2] + xs16[4 * q + 3];
-        return dA * fmaf(aA, TWO64, -8.f * XA) + dB * fmaf(aB, TWO64, -8.f * XB);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float dA = f16_bits_to_f32(U[r][0]);
+            const float dB = f16_bits_to_f32(U[r][4] >> 16);
+            acc[r] += dA * fmaf(a[r][0].x + a[r][0].y, TWO64, -8.f * XA) +
+                      dB * fmaf(a[r][1].x + a[r][1].y, TWO64, -8.f * XB);
+        }
     }
 };
 

@@ -1,0 +1,741 @@
+// prefill.cuh — the MoE FFN for many tokens at once ("aprender-serve 0.70.2 —
+// forward_qwen3_moe_resident.rs", moe_layer, applied to every token of a
+// batch; weights read once per batch as in apply_batch on "ferrox-core
+// 0.16.0 — weight_matrix.rs").  Tokens are grouped by routed expert and every
+// expert's gate/up and down products run as dense matrix products on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+//   pf_router_kernel   logits[T][E] = X R^T in f32 (CUDA cores)
+//   pf_topk_kernel     per token: softmax/top-k/renormalise, the (token, slot)
+//                      pairs appended to each expert's list, x copied to f16
+//                      with a power-of-two scale
+//   pf_gateup_kernel   per (expert, 128 features): D_g = G X^T, D_u = U X^T
+//                      (f16 x f16 -> f32); a[pair][f] = w * silu(g) * u
+//   pf_down_kernel     per (expert, 128 rows of H): D = Dn A^T (tf32 x tf32
+//                      -> f32); residual[t][i] += D  (atomic adds)
+//
+// Operand precision: gate/up weights are decoded exactly in f32 and rounded
+// once to f16; x is scaled per token by a power of two into f16's range and
+// rounded once.  Down weights and the activations are rounded to tf32 (round
+// to nearest).  Each product then carries at most 2 * 2^-11 relative error,
+// inside the 1e-3 * sum|w x| bound.  The down product's contributions of the
+// k experts are added to the residual with atomics, so their summation order
+// varies from run to run (within the same bound).
+#pragma once
+#include <cuda_fp16.h>
+
+#include "formats.cuh"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace qmoe {
+namespace pf {
+
+enum : unsigned { DEV_PF_TIMEOUT = 16, DEV_PF_RANGE = 17 };
+
+// ------------------------------------------------------------------ router
+// One thread per (token, expert): warp = 32 experts of one token.  The sum
+// runs in three levels (16 products, 16 of those, the rest) so its f32 error
+// stays near 40 ulp of sum |R x| whatever H is.
+constexpr int RT_TOK = 8;  // tokens per CTA (one per warp)
+
+__global__ void __launch_bounds__(256) pf_router_kernel(const float* __restrict__ R,
+                                                        const float* __restrict__ X, int T,
+                                                        int H, int E, float* __restrict__ logits,
+                                                        int32_t* __restrict__ cnt) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * RT_TOK + warp;
+    const int e = blockIdx.y * 32 + lane;
+    pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+    if (t >= T) return;
+    const float4* x4 = reinterpret_cast<const float4*>(X + static_cast<int64_t>(t) * H);
+    const float4* r4 = reinterpret_cast<const float4*>(R + static_cast<int64_t>(e < E ? e : 0) * H);
+    float total = 0.f;
+    for (int k0 = 0; k0 < H / 4; k0 += 64) {  // 256 elements
+        float mid = 0.f;
+        for (int k1 = k0; k1 < k0 + 64 && k1 < H / 4; k1 += 4) {  // 16 elements
+            float lo = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int kk = k1 + k;
+                if (kk < H / 4) {
+                    const float4 xv = __ldcg(x4 + kk), rv = __ldg(r4 + kk);
+                    lo = fmaf(xv.x, rv.x, lo);
+                    lo = fmaf(xv.y, rv.y, lo);
+                    lo = fmaf(xv.z, rv.z, lo);
+                    lo = fmaf(xv.w, rv.w, lo);
+                }
+            }
+            mid += lo;
+        }
+        total += mid;
+    }
+    if (e < E) logits[static_cast<int64_t>(t) * E + e] = total;
+}
+
+// ------------------------------------------------------------------ top-k
+// One warp per token.  Routing as the decode path (softmax over E, the k
+// largest with ties to the lower index, renormalised); each (token, slot)
+// pair is appended to its expert's list.  x is copied to f16 scaled by
+// 2^s_t, s_t chosen so that max |x| * 2^s_t lies in [2^14, 2^15).
+__global__ void __launch_bounds__(256) pf_topk_kernel(
+    const float* __restrict__ logits, const float* __restrict__ X, int T, int H, int E, int K,
+    int32_t* __restrict__ tidx, float* __restrict__ tw, int32_t* __restrict__ user_idx,
+    float* __restrict__ user_w, int32_t* __restrict__ cnt, int32_t* __restrict__ list,
+    __half* __restrict__ X16, float* __restrict__ xinv) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    pdl_wait();
+    pdl_trigger();
+    if (t >= T) return;
+    // logits of this token: lane holds experts lane, lane+32, ... (E <= 256)
+    float lv[8];
+    const float* lt = logits + static_cast<int64_t>(t) * E;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        lv[i] = e < E ? __ldcg(lt + e) : -INFINITY;
+    }
+    // rank of each of the lane's logits against all E
+    int rank[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rank[i] = 0;
+    for (int j = 0; j < 8; ++j) {
+        if (32 * j >= E) break;
+        for (int src = 0; src < 32; ++src) {
+            const float w = __shfl_sync(0xffffffffu, lv[j], src);
+            const int u = 32 * j + src;
+            if (u >= E) continue;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                rank[i] += (w > lv[i]) || (w == lv[i] && u < e);
+            }
+        }
+    }
+    // the selected experts, by rank: lane holding rank r publishes it
+    __shared__ int32_t s_idx[8][16];
+    __shared__ float s_l[8][16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && rank[i] < K) {
+            s_idx[warp][rank[i]] = e;
+            s_l[warp][rank[i]] = lv[i];
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        const float lmax = s_l[warp][0];
+        float p[16], z = 0.f;
+        for (int s = 0; s < K; ++s) {
+            p[s] = expf(s_l[warp][s] - lmax);
+            z += p[s];
+        }
+        const float inv = 1.0f / z;
+        for (int s = 0; s < K; ++s) {
+            const int e = s_idx[warp][s];
+            const float w = p[s] * inv;
+            const int64_t pair = static_cast<int64_t>(t) * K + s;
+            tidx[pair] = e;
+            tw[pair] = w;
+            if (user_idx) user_idx[pair] = e;
+            if (user_w) user_w[pair] = w;
+            const int pos = atomicAdd(&cnt[e], 1);
+            list[static_cast<int64_t>(e) * T + pos] = static_cast<int32_t>(pair);
+        }
+    }
+    // x -> f16 with a power-of-two scale
+    const float4* x4 = reinterpret_cast<const float4*>(X + static_cast<int64_t>(t) * H);
+    float amax = 0.f;
+    for (int i = lane; i < H / 4; i += 32) {
+        const float4 v = __ldcg(x4 + i);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int ex = 0;
+    if (amax > 0.f && isfinite(amax)) frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+    const int s = 15 - ex;
+    const float sc = ldexpf(1.0f, s);
+    if (lane == 0) xinv[t] = ldexpf(1.0f, -s);
+    __half2* o2 = reinterpret_cast<__half2*>(X16 + static_cast<int64_t>(t) * H);
+    for (int i = lane; i < H / 4; i += 32) {
+        const float4 v = __ldcg(x4 + i);
+        o2[2 * i] = __floats2half2_rn(v.x * sc, v.y * sc);
+        o2[2 * i + 1] = __floats2half2_rn(v.z * sc, v.w * sc);
+    }
+}
+
+// --------------------------------------------------------------- shared
+struct PfParams {
+    const uint8_t* W0;  // gate (gate/up kernel) or down stack
+    const uint8_t* W1;  // up stack
+    int64_t rb;         // row bytes of one weight row
+    int64_t es;         // expert stride in bytes
+    int H, F, E, K, T;
+    const int32_t* cnt;
+    const int32_t* list;
+    const __half* X16;
+    const float* xinv;
+    const float* tw;
+    float* a;         // [T*K][F] activations
+    float* residual;  // [T][H]
+    unsigned* err;
+};
+
+constexpr int PF_NP = 128;                // max tokens per pass (TMEM columns per region)
+constexpr int PF_WORKERS = 8;             // decode / B-load / epilogue warps
+constexpr int PF_THREADS = (2 + PF_WORKERS) * 32;
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// f32 -> tf32, round to nearest (ties away), kept in an f32 container.
+__device__ __forceinline__ float to_tf32(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+
+// --------------------------------------------------------- gate / up (f16)
+// Shared memory: raw Q4_K stages [2][256 rows][144 B]; A/B stages [2] of
+// { A_gate 128x64 f16, A_up 128x64 f16, B 128x64 f16 } (128-byte swizzled
+// K-major tiles, 1024-byte aligned); barriers; TMEM address.
+constexpr int GU_RAW_ROW = 144;
+constexpr int GU_RAW_STAGE = 256 * GU_RAW_ROW;      // 36,864
+constexpr int GU_TILE = 128 * 128;                  // 16,384 (128 rows x 128 B)
+constexpr int GU_AB_STAGE = 3 * GU_TILE;            // 49,152
+constexpr int GU_SMEM = 1024 + 2 * GU_AB_STAGE + 2 * GU_RAW_STAGE + 256;
+
+__global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ab = base;                               // 2 A/B stages
+    uint8_t* raw = base + 2 * GU_AB_STAGE;            // 2 raw stages
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + 2 * GU_RAW_STAGE);
+    uint64_t* raw_full = bars + 0;    // [2]
+    uint64_t* raw_empty = bars + 2;   // [2]
+    uint64_t* ab_full = bars + 4;     // [2]
+    uint64_t* ab_empty = bars + 6;    // [2]
+    uint64_t* acc_full = bars + 8;
+    uint64_t* acc_empty = bars + 9;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int FT = p.F / 128;              // feature tiles per expert
+    const int NB = p.H / 256;              // super-blocks per row
+    const int items = p.E * FT;
+
+    if (warp == 1) umma::tmem_alloc(tmem_slot, 256);
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], PF_WORKERS);
+            mbar_init(&ab_full[i], PF_WORKERS);
+            mbar_init(&ab_empty[i], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, PF_WORKERS);
+        fence_barrier_init();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        // -------------------------------------------- raw weight producer
+        const uint64_t pol = policy_evict_first();
+        int rit = 0;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            const int e = item / FT, ft = item % FT;
+            const int n = __ldcg(p.cnt + e);
+            if (n == 0) continue;
+            const int passes = (n + PF_NP - 1) / PF_NP;
+            for (int pass = 0; pass < passes; ++pass) {
+                for (int b = 0; b < NB; ++b, ++rit) {
+                    const int s = rit & 1, round = rit >> 1;
+                    if (round > 0 && !mbar_wait_bounded(&raw_empty[s], (round - 1) & 1, p.err,
+                                                        DEV_PF_TIMEOUT)) {
+                        // the stage's earlier copies completed (its consumers released
+                        // nothing further); wait for the other stage's copies, then leave
+                        mbar_wait_bounded(&raw_full[(s + 1) & 1], ((rit - 1) >> 1) & 1, p.err,
+                                          DEV_PF_TIMEOUT);
+                        return;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&raw_full[s], GU_RAW_STAGE);
+                    __syncwarp();
+                    for (int r = lane; r < 256; r += 32) {
+                        const uint8_t* m = r < 128 ? p.W0 : p.W1;
+                        const int f = ft * 128 + (r & 127);
+                        const uint8_t* src = m + static_cast<int64_t>(e) * p.es +
+                                             static_cast<int64_t>(f) * p.rb + b * GU_RAW_ROW;
+                        bulk_g2s(raw + s * GU_RAW_STAGE + r * GU_RAW_ROW, src, GU_RAW_ROW,
+                                 &raw_full[s], pol);
+                    }
+                }
+            }
+        }
+        // never leave with copies in flight: the last (up to two) stages
+        for (int k = rit - 2; k < rit; ++k)
+            if (k >= 0) mbar_wait_bounded(&raw_full[k & 1], (k >> 1) & 1, p.err, DEV_PF_TIMEOUT);
+        return;
+    }
+    if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int kit = 0, acc_round = 0;
+            for (int item = blockIdx.x; item < items; item += gridDim.x) {
+                const int e = item / FT;
+                const int n = __ldcg(p.cnt + e);
+                if (n == 0) continue;
+                const int passes = (n + PF_NP - 1) / PF_NP;
+                for (int pass = 0; pass < passes; ++pass, ++acc_round) {
+                    const int nt = min(PF_NP, n - pass * PF_NP);
+                    const int np = (nt + 15) & ~15;
+                    const uint32_t idesc = umma::idesc_f16(128, np);
+                    if (acc_round > 0 &&
+                        !mbar_wait_bounded(acc_empty, (acc_round - 1) & 1, p.err, DEV_PF_TIMEOUT)) {
+                        item = items;  // stop
+                        break;
+                    }
+                    umma::fence_after_sync();
+                    for (int kc = 0; kc < p.H / 64; ++kc, ++kit) {
+                        const int s = kit & 1, round = kit >> 1;
+                        if (!mbar_wait_bounded(&ab_full[s], round & 1, p.err, DEV_PF_TIMEOUT)) {
+                            item = items;
+                            pass = passes;
+                            break;
+                        }
+                        umma::fence_after_sync();
+                        const uint32_t st = smem_u32(ab + s * GU_AB_STAGE);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint64_t db = umma::desc_sw128(st + 2 * GU_TILE + 32 * j);
+                            const uint32_t acc = (kc > 0 || j > 0) ? 1u : 0u;
+                            umma::mma_f16(tmem, umma::desc_sw128(st + 32 * j), db, idesc, acc);
+                            umma::mma_f16(tmem + 128, umma::desc_sw128(st + GU_TILE + 32 * j), db,
+                                          idesc, acc);
+                        }
+                        umma::commit(&ab_empty[s]);
+                    }
+                    umma::commit(acc_full);
+                }
+            }
+        }
+        __syncwarp();
+        named_bar(1, (PF_WORKERS + 1) * 32);
+        umma::fence_after_sync();
+        umma::tmem_dealloc(tmem, 256);
+        return;
+    }
+
+    // --------------------------------------------------------------- workers
+    const int wk = warp - 2;              // 0..7
+    const int wt = tid - 64;              // 0..255
+    int kit = 0, rit = 0, acc_round = 0;
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int e = item / FT, ft = item % FT;
+        const int n = __ldcg(p.cnt + e);
+        if (n == 0) continue;
+        const int passes = (n + PF_NP - 1) / PF_NP;
+        const int32_t* lst = p.list + static_cast<int64_t>(e) * p.T;
+        for (int pass = 0; pass < passes; ++pass, ++acc_round) {
+            const int nt = min(PF_NP, n - pass * PF_NP);
+            const int np = (nt + 15) & ~15;
+            for (int kc = 0; kc < p.H / 64; ++kc, ++kit) {
+                const int s = kit & 1, round = kit >> 1;
+                if (round > 0 &&
+                    !mbar_wait_bounded(&ab_empty[s], (round - 1) & 1, p.err, DEV_PF_TIMEOUT))
+                    goto done;
+                uint8_t* st = ab + s * GU_AB_STAGE;
+                // B: rows j < np (tokens of this pass), 64 f16 of X16 at column kc*64
+                for (int c = wt; c < np * 8; c += 256) {
+                    const int j = c >> 3, ch = c & 7;
+                    if (j < nt) {
+                        const int pair = __ldcg(lst + pass * PF_NP + j);
+                        const int t = pair / p.K;
+                        const __half* src = p.X16 + static_cast<int64_t>(t) * p.H + kc * 64 + ch * 8;
+                        cp_async16(st + 2 * GU_TILE + umma::sw128_offset(j, ch * 16), src);
+                    } else {
+                        *reinterpret_cast<uint4*>(st + 2 * GU_TILE +
+                                                  umma::sw128_offset(j, ch * 16)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                // A: thread wt decodes quarter (kc % 4) of super-block kc/4 of row wt
+                const int qtr = kc & 3;
+                if (qtr == 0) {
+                    const int rs = rit & 1, rround = rit >> 1;
+                    if (!mbar_wait_bounded(&raw_full[rs], rround & 1, p.err, DEV_PF_TIMEOUT))
+                        goto done;
+                }
+                {
+                    const int rs = rit & 1;
+                    const uint8_t* sb = raw + rs * GU_RAW_STAGE + wt * GU_RAW_ROW;
+                    const uint4 hd = *reinterpret_cast<const uint4*>(sb);
+                    const float d = f16_bits_to_f32(hd.x), dmin = f16_bits_to_f32(hd.x >> 16);
+                    float sca, ma, scb, mb;
+                    FmtQ4K::scale_min(hd.y, hd.z, hd.w, qtr, sca, ma, scb, mb);
+                    const float d1 = d * sca, m1 = dmin * ma, d2 = d * scb, m2 = dmin * mb;
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(sb + 16 + 32 * qtr);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(sb + 16 + 32 * qtr + 16);
+                    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    // element 64*qtr + l (low nibble of byte l) and +32 (high nibble)
+                    uint8_t* arow = st + (wt < 128 ? 0 : GU_TILE);
+                    const int r = wt & 127;
+                    float rng = 0.f;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {       // low nibbles, then high
+                        const float dd = hh ? d2 : d1, mm = hh ? m2 : m1;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {      // 16-byte chunks: 8 values
+                            uint32_t h2[4];
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const uint32_t w = qw[2 * c + (v >> 1)];
+                                const int sh = 16 * (v & 1) + 4 * hh;
+                                const float a0 = fmaf(dd, static_cast<float>((w >> sh) & 15u), -mm);
+                                const float a1 =
+                                    fmaf(dd, static_cast<float>((w >> (sh + 8)) & 15u), -mm);
+                                rng = fmaxf(rng, fmaxf(fabsf(a0), fabsf(a1)));
+                                const __half2 hv = __floats2half2_rn(a0, a1);
+                                h2[v] = *reinterpret_cast<const uint32_t*>(&hv);
+                            }
+                            // values l = 8c..8c+7 of this half; column 32*hh + 8c
+                            const int col = 32 * hh + 8 * c;
+                            *reinterpret_cast<uint4*>(arow + umma::sw128_offset(r, col * 2)) =
+                                make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                        }
+                    }
+                    if (rng > 65504.f && rng < INFINITY) atomicCAS(p.err, 0u, DEV_PF_RANGE);
+                }
+                if (qtr == 3) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&raw_empty[rit & 1]);
+                    ++rit;
+                }
+                cp_async_wait_all();
+                umma::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ab_full[s]);
+            }
+            // ---- epilogue: a[pair][f] = w * silu(g) * u
+            if (!mbar_wait_bounded(acc_full, acc_round & 1, p.err, DEV_PF_TIMEOUT)) goto done;
+            umma::fence_after_sync();
+            const int lq = warp & 3;               // TMEM lane quarter of this warp
+            const int f = ft * 128 + 32 * lq + lane;
+            const int c0 = (wk < 4) ? 0 : np / 2;  // two warpgroups split the columns
+            const int c1 = (wk < 4) ? np / 2 : np;
+            for (int cb = c0; cb < c1; cb += 16) {
+                float g[16], u[16];
+                umma::ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + cb, g);
+                umma::ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + 128 + cb, u);
+                umma::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int j = cb + i;
+                    if (j < nt && j < c1) {
+                        const int pair = __ldcg(lst + pass * PF_NP + j);
+                        const int t = pair / p.K;
+                        const float xi = __ldcg(p.xinv + t);
+                        const float gv = g[i] * xi, uv = u[i] * xi;
+                        p.a[static_cast<int64_t>(pair) * p.F + f] =
+                            __ldcg(p.tw + pair) * ((gv / (1.0f + expf(-gv))) * uv);
+                    }
+                }
+            }
+            umma::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+    }
+done:
+    // the allocating warp frees tensor memory once every worker is past its
+    // last tensor-memory read
+    umma::fence_before_sync();
+    __syncwarp();
+    named_bar(1, (PF_WORKERS + 1) * 32);
+}
+
+// ------------------------------------------------------------- down (tf32)
+// Shared memory: raw Q6_K stages [2][128 rows][240 B] (16-byte-aligned copies
+// of each 210-byte super-block); A/B stages [2] of { A 128x32 tf32, B
+// 128x32 tf32 } swizzled; barriers; TMEM address.
+constexpr int DN_RAW_ROW = 240;
+constexpr int DN_RAW_STAGE = 128 * DN_RAW_ROW;      // 30,720
+constexpr int DN_TILE = 128 * 128;                  // 16,384
+constexpr int DN_AB_STAGE = 2 * DN_TILE;            // 32,768
+constexpr int DN_SMEM = 1024 + 2 * DN_AB_STAGE + 2 * DN_RAW_STAGE + 256;
+
+__global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ab = base;
+    uint8_t* raw = base + 2 * DN_AB_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + 2 * DN_RAW_STAGE);
+    uint64_t* raw_full = bars + 0;
+    uint64_t* raw_empty = bars + 2;
+    uint64_t* ab_full = bars + 4;
+    uint64_t* ab_empty = bars + 6;
+    uint64_t* acc_full = bars + 8;
+    uint64_t* acc_empty = bars + 9;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int MT = p.H / 128;              // row tiles per expert
+    const int NB = p.F / 256;              // super-blocks per row
+    const int items = p.E * MT;
+
+    if (warp == 1) umma::tmem_alloc(tmem_slot, 128);
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], PF_WORKERS);
+            mbar_init(&ab_full[i], PF_WORKERS);
+            mbar_init(&ab_empty[i], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, PF_WORKERS);
+        fence_barrier_init();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        const uint64_t pol = policy_evict_first();
+        int rit = 0;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            const int e = item / MT, mt = item % MT;
+            const int n = __ldcg(p.cnt + e);
+            if (n == 0) continue;
+            const int passes = (n + PF_NP - 1) / PF_NP;
+            for (int pass = 0; pass < passes; ++pass) {
+                for (int b = 0; b < NB; ++b, ++rit) {
+                    const int s = rit & 1, round = rit >> 1;
+                    if (round > 0 && !mbar_wait_bounded(&raw_empty[s], (round - 1) & 1, p.err,
+                                                        DEV_PF_TIMEOUT)) {
+                        // the stage's earlier copies completed (its consumers released
+                        // nothing further); wait for the other stage's copies, then leave
+                        mbar_wait_bounded(&raw_full[(s + 1) & 1], ((rit - 1) >> 1) & 1, p.err,
+                                          DEV_PF_TIMEOUT);
+                        return;
+                    }
+                    // per-row 16-byte-aligned windows around each 210-byte block
+                    uint32_t mine = 0;
+                    for (int r = lane; r < 128; r += 32) {
+                        const uintptr_t src = reinterpret_cast<uintptr_t>(
+                            p.W0 + static_cast<int64_t>(e) * p.es +
+                            static_cast<int64_t>(mt * 128 + r) * p.rb + b * 210);
+                        const uintptr_t lo = src & ~uintptr_t(15);
+                        mine += static_cast<uint32_t>(((src + 210 + 15) & ~uintptr_t(15)) - lo);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+                    if (lane == 0) mbar_arrive_expect_tx(&raw_full[s], mine);
+                    __syncwarp();
+                    for (int r = lane; r < 128; r += 32) {
+                        const uintptr_t src = reinterpret_cast<uintptr_t>(
+                            p.W0 + static_cast<int64_t>(e) * p.es +
+                            static_cast<int64_t>(mt * 128 + r) * p.rb + b * 210);
+                        const uintptr_t lo = src & ~uintptr_t(15);
+                        const uint32_t nbytes =
+                            static_cast<uint32_t>(((src + 210 + 15) & ~uintptr_t(15)) - lo);
+                        bulk_g2s(raw + s * DN_RAW_STAGE + r * DN_RAW_ROW,
+                                 reinterpret_cast<const void*>(lo), nbytes, &raw_full[s], pol);
+                    }
+                }
+            }
+        }
+        for (int k = rit - 2; k < rit; ++k)
+            if (k >= 0) mbar_wait_bounded(&raw_full[k & 1], (k >> 1) & 1, p.err, DEV_PF_TIMEOUT);
+        return;
+    }
+    if (warp == 1) {
+        if (lane == 0) {
+            int kit = 0, acc_round = 0;
+            for (int item = blockIdx.x; item < items; item += gridDim.x) {
+                const int e = item / MT;
+                const int n = __ldcg(p.cnt + e);
+                if (n == 0) continue;
+                const int passes = (n + PF_NP - 1) / PF_NP;
+                for (int pass = 0; pass < passes; ++pass, ++acc_round) {
+                    const int nt = min(PF_NP, n - pass * PF_NP);
+                    const int np = (nt + 15) & ~15;
+                    const uint32_t idesc = umma::idesc_tf32(128, np);
+                    if (acc_round > 0 &&
+                        !mbar_wait_bounded(acc_empty, (acc_round - 1) & 1, p.err, DEV_PF_TIMEOUT)) {
+                        item = items;  // stop
+                        break;
+                    }
+                    umma::fence_after_sync();
+                    for (int kc = 0; kc < p.F / 32; ++kc, ++kit) {
+                        const int s = kit & 1, round = kit >> 1;
+                        if (!mbar_wait_bounded(&ab_full[s], round & 1, p.err, DEV_PF_TIMEOUT)) {
+                            item = items;
+                            pass = passes;
+                            break;
+                        }
+                        umma::fence_after_sync();
+                        const uint32_t st = smem_u32(ab + s * DN_AB_STAGE);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            umma::mma_tf32(tmem, umma::desc_sw128(st + 32 * j),
+                                           umma::desc_sw128(st + DN_TILE + 32 * j), idesc,
+                                           (kc > 0 || j > 0) ? 1u : 0u);
+                        umma::commit(&ab_empty[s]);
+                    }
+                    umma::commit(acc_full);
+                }
+            }
+        }
+        __syncwarp();
+        named_bar(1, (PF_WORKERS + 1) * 32);
+        umma::fence_after_sync();
+        umma::tmem_dealloc(tmem, 128);
+        return;
+    }
+
+    const int wk = warp - 2;
+    const int wt = tid - 64;
+    int kit = 0, rit = 0, acc_round = 0;
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int e = item / MT, mt = item % MT;
+        const int n = __ldcg(p.cnt + e);
+        if (n == 0) continue;
+        const int passes = (n + PF_NP - 1) / PF_NP;
+        const int32_t* lst = p.list + static_cast<int64_t>(e) * p.T;
+        for (int pass = 0; pass < passes; ++pass, ++acc_round) {
+            const int nt = min(PF_NP, n - pass * PF_NP);
+            const int np = (nt + 15) & ~15;
+            for (int kc = 0; kc < p.F / 32; ++kc, ++kit) {
+                const int s = kit & 1, round = kit >> 1;
+                if (round > 0 &&
+                    !mbar_wait_bounded(&ab_empty[s], (round - 1) & 1, p.err, DEV_PF_TIMEOUT))
+                    goto done;
+                uint8_t* st = ab + s * DN_AB_STAGE;
+                // B: activations a[pair][kc*32 .. +32] rounded to tf32
+                for (int c = wt; c < np * 8; c += 256) {
+                    const int j = c >> 3, ch = c & 7;
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (j < nt) {
+                        const int pair = __ldcg(lst + pass * PF_NP + j);
+                        v = __ldcg(reinterpret_cast<const float4*>(
+                            p.a + static_cast<int64_t>(pair) * p.F + kc * 32 + ch * 4));
+                        v.x = to_tf32(v.x);
+                        v.y = to_tf32(v.y);
+                        v.z = to_tf32(v.z);
+                        v.w = to_tf32(v.w);
+                    }
+                    *reinterpret_cast<float4*>(st + DN_TILE + umma::sw128_offset(j, ch * 16)) = v;
+                }
+                // A: row r = wt/2, 16 values (half hh) of the 32-element chunk
+                const int sbk = kc & 7;            // chunk within the super-block
+                if (sbk == 0) {
+                    const int rs = rit & 1, rround = rit >> 1;
+                    if (!mbar_wait_bounded(&raw_full[rs], rround & 1, p.err, DEV_PF_TIMEOUT))
+                        goto done;
+                }
+                {
+                    const int rs = rit & 1;
+                    const int r = wt >> 1, hh = wt & 1;
+                    const uintptr_t src = reinterpret_cast<uintptr_t>(
+                        p.W0 + static_cast<int64_t>(e) * p.es +
+                        static_cast<int64_t>(mt * 128 + r) * p.rb + (kc >> 3) * 210);
+                    const uint8_t* sb = raw + rs * DN_RAW_STAGE + r * DN_RAW_ROW + (src & 15u);
+                    // chunk sbk = (half h, quarter t) of the super-block: elements
+                    // 128h + 32t + l, l in [16hh, 16hh + 16)
+                    const int h = sbk >> 2, t = sbk & 3;
+                    uint32_t QL[4], QH[4];
+                    load4_u16al(sb + 64 * h + 32 * (t & 1) + 16 * hh, QL);
+                    load4_u16al(sb + 128 + 32 * h + 16 * hh, QH);
+                    const uintptr_t da = reinterpret_cast<uintptr_t>(sb + 208);
+                    const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
+                    const float d = f16_bits_to_f32(dw >> ((da & 3u) * 8u));
+                    const uintptr_t sa = reinterpret_cast<uintptr_t>(sb + 192 + 8 * h + hh + 2 * t);
+                    const uint32_t sw = *reinterpret_cast<const uint32_t*>(sa & ~uintptr_t(3));
+                    const float scl = static_cast<float>(static_cast<int8_t>(sw >> ((sa & 3u) * 8u)));
+                    const float ds = d * scl;
+                    float vals[16];
+#pragma unroll
+                    for (int wv = 0; wv < 4; ++wv) {
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb) {
+                            const uint32_t lo4 = (QL[wv] >> (8 * bb + 4 * (t >> 1))) & 15u;
+                            const uint32_t hi2 = (QH[wv] >> (8 * bb + 2 * t)) & 3u;
+                            const int q = static_cast<int>(lo4 | (hi2 << 4)) - 32;
+                            vals[4 * wv + bb] = to_tf32(ds * static_cast<float>(q));
+                        }
+                    }
+                    uint8_t* arow = st;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int col = 16 * hh + 4 * c;   // tf32 column in the 32-wide chunk
+                        *reinterpret_cast<float4*>(arow + umma::sw128_offset(r, col * 4)) =
+                            make_float4(vals[4 * c], vals[4 * c + 1], vals[4 * c + 2],
+                                        vals[4 * c + 3]);
+                    }
+                }
+                if (sbk == 7) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&raw_empty[rit & 1]);
+                    ++rit;
+                }
+                umma::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ab_full[s]);
+            }
+            // ---- epilogue: residual[t][i] += D[i][j]
+            if (!mbar_wait_bounded(acc_full, acc_round & 1, p.err, DEV_PF_TIMEOUT)) goto done;
+            umma::fence_after_sync();
+            const int lq = warp & 3;
+            const int i = mt * 128 + 32 * lq + lane;
+            const int c0 = (wk < 4) ? 0 : np / 2;
+            const int c1 = (wk < 4) ? np / 2 : np;
+            for (int cb = c0; cb < c1; cb += 16) {
+                float dv[16];
+                umma::ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + cb, dv);
+                umma::wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int j = cb + k;
+                    if (j < nt && j < c1) {
+                        const int pair = __ldcg(lst + pass * PF_NP + j);
+                        const int t = pair / p.K;
+                        atomicAdd(p.residual + static_cast<int64_t>(t) * p.H + i, dv[k]);
+                    }
+                }
+            }
+            umma::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+    }
+done:
+    // the allocating warp frees tensor memory once every worker is past its
+    // last tensor-memory read
+    umma::fence_before_sync();
+    __syncwarp();
+    named_bar(1, (PF_WORKERS + 1) * 32);
+}
+
+}  // namespace pf
+}  // namespace qmoe

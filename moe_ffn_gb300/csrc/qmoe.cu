@@ -13,6 +13,7 @@
 #include "formats.cuh"
 #include "ptx.cuh"
 #include "stream.cuh"
+#include "prefill.cuh"
 
 namespace qmoe {
 
@@ -143,12 +144,12 @@ static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cud
 template <class Fmt, int MODE>
 static bool plan(StreamParams& p, int smem_optin, int* smem_bytes) {
     using G = ModeGeom<MODE>;
-    // stage budget: at most 48 KB, and at least two stages must fit beside
+    // stage budget: at most 96 KB, and at least two stages must fit beside
     // the x' table
     p.stage_bytes = 0;
     p.nstages = 0;
     const int room = smem_optin - smem_layout(p).total;
-    int budget = room / 2 < 48 * 1024 ? room / 2 : 48 * 1024;
+    int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
     if (budget < G::ROWS * (Fmt::SBB + 31)) return false;
     const int seg_full = p.nb_seg * Fmt::SBB;
     const int piece_full = align_up(seg_full + 15, 16);
@@ -414,11 +415,110 @@ static size_t moe_logits_bytes(const qmoe_moe_shape* s) {
     return static_cast<size_t>(align_up(s->n_tokens * s->num_experts * 4, 256));
 }
 
+// Token count from which the grouped tensor-core path is used (for the
+// formats it implements); below it tokens run the decode pipeline one by one.
+constexpr int PF_MIN_TOKENS = 32;
+
+static bool prefill_path(const qmoe_moe_shape* s) {
+    return s->n_tokens >= PF_MIN_TOKENS && s->gate_qtype == QT_Q4_K && s->up_qtype == QT_Q4_K &&
+           s->down_qtype == QT_Q6_K && s->expert_dim % 256 == 0 && s->hidden % 256 == 0;
+}
+
+// Prefill workspace carve-up (byte offsets from ws).
+struct PfWs {
+    size_t logits, tidx, tw, cnt, list, x16, xinv, a, total;
+};
+static PfWs pf_ws_layout(const qmoe_moe_shape* s) {
+    const size_t T = s->n_tokens, E = s->num_experts, K = s->top_k, H = s->hidden,
+                 F = s->expert_dim;
+    auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+    PfWs w;
+    size_t o = 0;
+    w.logits = o; o += al(T * E * 4);
+    w.tidx = o;   o += al(T * K * 4);
+    w.tw = o;     o += al(T * K * 4);
+    w.cnt = o;    o += al(E * 4);
+    w.list = o;   o += al(E * T * 4);
+    w.x16 = o;    o += al(T * H * 2);
+    w.xinv = o;   o += al(T * 4);
+    w.a = o;      o += al(T * K * F * 4);
+    w.total = o;
+    return w;
+}
+
 size_t moe_ffn_workspace_size(const qmoe_moe_shape* s) {
-    if (!s || s->n_tokens <= 0 || s->num_experts <= 0 || s->top_k <= 0 || s->expert_dim <= 0)
+    if (!s || s->n_tokens <= 0 || s->num_experts <= 0 || s->top_k <= 0 || s->expert_dim <= 0 ||
+        s->hidden <= 0)
         return 0;
-    return moe_logits_bytes(s) +
-           static_cast<size_t>(align_up(s->top_k * s->expert_dim * 4, 256));
+    const size_t decode = moe_logits_bytes(s) +
+                          static_cast<size_t>(align_up(s->top_k * s->expert_dim * 4, 256));
+    if (prefill_path(s)) {
+        const size_t pf = pf_ws_layout(s).total;
+        return pf > decode ? pf : decode;
+    }
+    return decode;
+}
+
+static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
+                               const void* up_stack, const void* down_stack,
+                               const qmoe_moe_shape& s, const float* x, float* residual,
+                               int32_t* topk_idx, float* topk_w, void* ws, const DevInfo& d,
+                               cudaStream_t st) {
+    const PfWs L = pf_ws_layout(&s);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* logits = reinterpret_cast<float*>(w + L.logits);
+    int32_t* tidx = reinterpret_cast<int32_t*>(w + L.tidx);
+    float* tw = reinterpret_cast<float*>(w + L.tw);
+    int32_t* cnt = reinterpret_cast<int32_t*>(w + L.cnt);
+    int32_t* list = reinterpret_cast<int32_t*>(w + L.list);
+    __half* x16 = reinterpret_cast<__half*>(w + L.x16);
+    float* xinv = reinterpret_cast<float*>(w + L.xinv);
+    float* a = reinterpret_cast<float*>(w + L.a);
+    const int T = s.n_tokens, H = s.hidden, E = s.num_experts, K = s.top_k, F = s.expert_dim;
+
+    cudaError_t e = launch_pdl(pf::pf_router_kernel, dim3((T + 7) / 8, (E + 31) / 32), dim3(256),
+                               0, st, router_W, x, T, H, E, logits, cnt);
+    if (e != cudaSuccess) return cuda_fail(e, "pf_router launch");
+    e = launch_pdl(pf::pf_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st,
+                   static_cast<const float*>(logits), x, T, H, E, K, tidx, tw, topk_idx, topk_w,
+                   cnt, list, x16, xinv);
+    if (e != cudaSuccess) return cuda_fail(e, "pf_topk launch");
+
+    static int configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!configured[dev & 63]) {
+        e = cudaFuncSetAttribute(pf::pf_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 pf::GU_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(pf::pf_down_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, pf::DN_SMEM);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
+        configured[dev & 63] = 1;
+    }
+    pf::PfParams pg = {};
+    pg.W0 = static_cast<const uint8_t*>(gate_stack);
+    pg.W1 = static_cast<const uint8_t*>(up_stack);
+    pg.rb = row_bytes_of(QT_Q4_K, H);
+    pg.es = pg.rb * F;
+    pg.H = H; pg.F = F; pg.E = E; pg.K = K; pg.T = T;
+    pg.cnt = cnt; pg.list = list; pg.X16 = x16; pg.xinv = xinv; pg.tw = tw; pg.a = a;
+    pg.residual = residual;
+    pg.err = d.err;
+    const int items_gu = E * (F / 128);
+    e = launch_pdl(pf::pf_gateup_kernel, dim3(items_gu < d.sms ? items_gu : d.sms),
+                   dim3(pf::PF_THREADS), static_cast<size_t>(pf::GU_SMEM), st, pg);
+    if (e != cudaSuccess) return cuda_fail(e, "pf_gateup launch");
+    pf::PfParams pd = pg;
+    pd.W0 = static_cast<const uint8_t*>(down_stack);
+    pd.W1 = nullptr;
+    pd.rb = row_bytes_of(QT_Q6_K, F);
+    pd.es = pd.rb * H;
+    const int items_dn = E * (H / 128);
+    e = launch_pdl(pf::pf_down_kernel, dim3(items_dn < d.sms ? items_dn : d.sms),
+                   dim3(pf::PF_THREADS), static_cast<size_t>(pf::DN_SMEM), st, pd);
+    if (e != cudaSuccess) return cuda_fail(e, "pf_down launch");
+    return QMOE_OK;
 }
 
 qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* up_stack,
@@ -463,6 +563,10 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
     DevInfo* d = nullptr;
     if (qmoe_status st = device_info(&d)) return st;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (prefill_path(&s))
+        return run_prefill(router_W, gate_stack, up_stack, down_stack, s, x, residual, topk_idx,
+                           topk_w, ws, *d, st);
 
     const int H = s.hidden, F = s.expert_dim, E = s.num_experts, K = s.top_k;
     float* logits = static_cast<float*>(ws);

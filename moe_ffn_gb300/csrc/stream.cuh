@@ -1,13 +1,16 @@
 // stream.cuh — the streaming decode GEMV engine shared by qmv, ffn_swiglu and
-// moe_ffn (T = 1 decode).
+// moe_ffn (decode).
 //
 // One CTA per SM (persistent over a contiguous range of output units).
 // Warp 8 is the producer: it stages weight rows into a ring of shared-memory
 // stages with 1-D bulk TMA copies (cp.async.bulk, completion counted on an
-// mbarrier).  Warps 0..7 are consumers: lane (g = lane/4, q = lane%4) owns
-// row g of its warp's 8-row subtile and quarter q of every 256-element
-// group it is given; per-row partial sums are reduced by shuffles across the
-// four quarters and through shared memory across warps, in a fixed order.
+// mbarrier).  Warps 0..7 are consumers.  A tile holds 8*R row slots; lane
+// (g = lane/4, q = lane%4) owns slots rr*8 + g (rr < R) and quarter q of each
+// 256-element group its warp is given: warp v takes groups v, v+8, ... of
+// the chunk.  A lane loads its 64 x' values of a group into registers once
+// and applies them to its R rows.  Per-row partial sums are reduced by
+// shuffles across the four quarters and through shared memory across warps,
+// in a fixed order (deterministic).
 //
 // Weight operands are read-only constants: the producer starts streaming
 // them before griddepcontrol.wait, so a launch overlaps the tail of the
@@ -15,10 +18,11 @@
 // wait.
 //
 // Modes:
-//   QMV     y[r] = W[r] . x                         (overwrite)
-//   GATEUP  a[j] = w_s * silu(G_e[jj].x) * (U_e[jj].x),  j = s*F + jj
-//           (dense: one slot, w = 1)
-//   DOWN    residual[i] += sum_s D_e_s[i] . a_s      (k-segments = slots)
+//   QMV     y[r] = W[r] . x                         (overwrite)           R = 4
+//   GATEUP  a[j] = w_s * silu(G_e[jj].x) * (U_e[jj].x),  j = s*F + jj      R = 4
+//           (slots rr = 0,1 gate rows, rr = 2,3 up rows of the same units;
+//            dense: one slot, w = 1)
+//   DOWN    residual[i] += sum_s D_e_s[i] . a_s      (k-segments = slots)  R = 2
 #pragma once
 #include "formats.cuh"
 #include "ptx.cuh"
@@ -30,6 +34,7 @@ constexpr int NTHREADS = (NCW + 1) * 32;  // + producer warp
 constexpr int MAX_STAGES = 4;
 constexpr int MAX_EXPERTS = 256;
 constexpr int MAX_TOPK = 16;
+constexpr int MAX_ROWS = 32;              // row slots per tile (8 * R)
 
 enum Mode : int { MODE_QMV = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
 
@@ -60,6 +65,13 @@ struct StreamParams {
     unsigned* err;
 };
 
+template <int MODE> struct ModeGeom {
+    static constexpr int R = (MODE == MODE_DOWN) ? 2 : 4;  // row slots per lane
+    static constexpr int ROWS = 8 * R;                     // row slots per tile
+    static constexpr int TU = (MODE == MODE_GATEUP) ? ROWS / 2 : ROWS;  // units per tile
+    static constexpr int WK = NCW;                         // warps along K
+};
+
 // Shared-memory carve-up (dynamic): [barriers][topk][part][xs16][xq][stages]
 struct SmemLayout {
     int off_full, off_empty, off_tidx, off_tw, off_logit, off_part, off_xs, off_xq, off_stage,
@@ -76,7 +88,7 @@ __host__ __device__ inline SmemLayout smem_layout(const StreamParams& p) {
     L.off_tidx = o;  o += 4 * MAX_TOPK;
     L.off_tw = o;    o += 4 * MAX_TOPK;
     L.off_logit = o; o += 4 * MAX_EXPERTS;
-    L.off_part = o;  o += 4 * 2 * NCW * 16;
+    L.off_part = o;  o += 4 * 2 * NCW * MAX_ROWS;
     o = align_up(o, 16);
     L.off_xs = o;    o += 4 * 16 * p.nb_seg * p.n_kseg;
     o = align_up(o, 128);
@@ -87,12 +99,6 @@ __host__ __device__ inline SmemLayout smem_layout(const StreamParams& p) {
     L.total = o;
     return L;
 }
-
-template <int MODE> struct ModeGeom {
-    static constexpr int SUB = (MODE == MODE_GATEUP) ? 2 : 1;  // 8-row subtiles per tile
-    static constexpr int WK = NCW / SUB;                       // warps along K
-    static constexpr int ROWS = 8 * SUB;                       // row slots per tile
-};
 
 // Routing: softmax over the E logits, the k largest (ties: lower index),
 // renormalised over those k — the page's "softmax, top-k, renormalize" of
@@ -196,16 +202,15 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
 }
 
 // Address of the bytes of (row slot r, k-segment ks) for the tile starting
-// at unit u0; nullptr if the row is outside the CTA's range.
+// at unit u0; nullptr if the row's unit is outside [.., uend).
 template <int MODE>
 __device__ __forceinline__ const uint8_t* row_addr(const StreamParams& p, const int32_t* s_idx,
                                                    int64_t u0, int64_t uend, int r, int ks) {
-    const int g = r & 7;
-    const int64_t u = u0 + g;
-    if (u >= uend) return nullptr;
-    if (MODE == MODE_QMV) return p.W0 + u * p.rb0;
+    const int g = r & 7, rr = r >> 3;
     if (MODE == MODE_GATEUP) {
-        const bool up = r >= 8;
+        const bool up = rr >= 2;
+        const int64_t u = u0 + (rr & 1) * 8 + g;
+        if (u >= uend) return nullptr;
         const uint8_t* base = up ? p.W1 : p.W0;
         const int64_t rb = up ? p.rb1 : p.rb0, es = up ? p.es1 : p.es0;
         if (p.moe) {
@@ -215,6 +220,9 @@ __device__ __forceinline__ const uint8_t* row_addr(const StreamParams& p, const 
         }
         return base + u * rb;
     }
+    const int64_t u = u0 + r;
+    if (u >= uend) return nullptr;
+    if (MODE == MODE_QMV) return p.W0 + u * p.rb0;
     // DOWN
     if (p.moe) return p.W0 + static_cast<int64_t>(s_idx[ks]) * p.es0 + u * p.rb0;
     return p.W0 + u * p.rb0;
@@ -243,6 +251,7 @@ __device__ __forceinline__ ChunkDesc chunk_desc(const StreamParams& p, int c) {
 template <class Fmt, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamParams p) {
     using G = ModeGeom<MODE>;
+    constexpr int R = G::R;
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = smem_layout(p);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
@@ -284,14 +293,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
         __syncthreads();
     }
 
-    const int ntiles = static_cast<int>((uend - ubeg + 7) / 8);
+    const int ntiles = static_cast<int>((uend - ubeg + G::TU - 1) / G::TU);
 
     if (warp == NCW) {
         // ------------------------------------------------------ producer
         const uint64_t pol = policy_evict_first();
         int it = 0;
         for (int t = 0; t < ntiles; ++t) {
-            const int64_t u0 = ubeg + 8 * static_cast<int64_t>(t);
+            const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
             for (int c = 0; c < p.n_chunk; ++c, ++it) {
                 const int s = it % p.nstages;
                 const int round = it / p.nstages;
@@ -301,7 +310,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
                 const ChunkDesc cd = chunk_desc(p, c);
                 const int ncopy = G::ROWS * cd.nks;
                 const uint32_t seg_bytes = static_cast<uint32_t>(cd.nbp * Fmt::SBB);
-                // total bytes of this stage's copies
                 uint32_t mine = 0;
                 for (int k = lane; k < ncopy; k += 32) {
                     const int r = k / cd.nks, pk = k % cd.nks;
@@ -344,16 +352,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
     build_xprime<Fmt>(p.x, p.nb_seg * p.n_kseg, xq, xs, tid, NCW * 32);
     named_bar(1, NCW * 32);
 
-    const int u_sub = warp / G::WK, v = warp % G::WK;
+    const int v = warp;
     const int g = lane >> 2, q = lane & 3;
-    const int r = u_sub * 8 + g;
     const float4* xq4 = reinterpret_cast<const float4*>(xq);
     int it = 0;
     bool ok = true;
     for (int t = 0; t < ntiles && ok; ++t) {
-        const int64_t u0 = ubeg + 8 * static_cast<int64_t>(t);
-        const int nu = static_cast<int>(uend - u0 < 8 ? uend - u0 : 8);
-        float acc = 0.f;
+        const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
+        float acc[R];
+        // low 32 bits of each row's address (k-segment 0): only the 16-byte
+        // phase is needed to find the row inside its staged slot
+        uint32_t rowlo[R];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            acc[rr] = 0.f;
+            const uint8_t* a = row_addr<MODE>(p, s_idx, u0, uend, rr * 8 + g, 0);
+            rowlo[rr] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a));
+            if (MODE == MODE_DOWN && p.moe && a)  // k-segment 0's expert offset removed
+                rowlo[rr] -= static_cast<uint32_t>(s_idx[0]) * static_cast<uint32_t>(p.es0);
+        }
         for (int c = 0; c < p.n_chunk; ++c, ++it) {
             const int s = it % p.nstages;
             const int round = it / p.nstages;
@@ -363,49 +380,61 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
             }
             const ChunkDesc cd = chunk_desc(p, c);
             const uint8_t* st = stages + static_cast<size_t>(s) * p.stage_bytes;
-            if (g < nu) {
-                const int ntot = cd.nks * cd.nbp;
-                for (int tt = v; tt < ntot; tt += G::WK) {
-                    const int pk = tt / cd.nbp, bb = tt - pk * cd.nbp;
-                    const int ks = cd.ks0 + pk, b = cd.b0 + bb;
-                    const uint8_t* a = row_addr<MODE>(p, s_idx, u0, uend, r, ks);
-                    const uintptr_t src = reinterpret_cast<uintptr_t>(a) +
-                                          static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
-                    const int delta = static_cast<int>(src & 15u);
-                    const uint8_t* sb =
-                        st + r * p.slot_stride + pk * p.piece_stride + delta + bb * Fmt::SBB;
-                    const int gidx = ks * p.nb_seg + b;
-                    acc += Fmt::dot(sb, q, xq4 + gidx * 64, xs + gidx * 16);
+            const int ntot = cd.nks * cd.nbp;
+            const uint32_t b0off = static_cast<uint32_t>(cd.b0) * Fmt::SBB;
+            for (int tt = v; tt < ntot; tt += G::WK) {
+                const int pk = tt / cd.nbp, bb = tt - pk * cd.nbp;
+                const int ks = cd.ks0 + pk, b = cd.b0 + bb;
+                const int gidx = ks * p.nb_seg + b;
+                float x[64];
+                load_xq(xq4 + gidx * 64, q, x);
+                const float* xsg = xs + gidx * 16;
+                const uint32_t ksoff =
+                    (MODE == MODE_DOWN && p.moe)
+                        ? static_cast<uint32_t>(s_idx[ks]) * static_cast<uint32_t>(p.es0)
+                        : 0u;
+                // rows outside the CTA's range read (in-bounds, stale) slot
+                // bytes; their sums are never written out
+                const uint8_t* sbp[R];
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr) {
+                    const int delta = static_cast<int>((rowlo[rr] + ksoff + b0off) & 15u);
+                    sbp[rr] = st + (rr * 8 + g) * p.slot_stride + pk * p.piece_stride + delta +
+                              bb * Fmt::SBB;
                 }
+                Fmt::template dotR<R>(sbp, q, x, xsg, acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
         if (!ok) break;
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        float* pt = part + (t & 1) * NCW * 16;
-        if (q == 0) pt[v * 16 + r] = acc;
+        float* pt = part + (t & 1) * NCW * MAX_ROWS;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            float a = acc[rr];
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            if (q == 0) pt[v * MAX_ROWS + rr * 8 + g] = a;
+        }
         named_bar(1, NCW * 32);
         const int ct = tid;
-        if (ct < nu) {
+        if (ct < G::TU && u0 + ct < uend) {
             const int64_t u = u0 + ct;
-            if (MODE == MODE_QMV) {
-                float y = 0.f;
-                for (int k = 0; k < G::WK; ++k) y += pt[k * 16 + ct];
-                p.out[u] = y;
-            } else if (MODE == MODE_GATEUP) {
+            if (MODE == MODE_GATEUP) {
                 float gs = 0.f, us = 0.f;
                 for (int k = 0; k < G::WK; ++k) {
-                    gs += pt[k * 16 + ct];
-                    us += pt[k * 16 + 8 + ct];
+                    gs += pt[k * MAX_ROWS + ct];
+                    us += pt[k * MAX_ROWS + G::TU + ct];
                 }
                 const float w = p.moe ? s_w[static_cast<int>(u / p.F)] : 1.0f;
                 p.out[u] = w * ((gs / (1.0f + expf(-gs))) * us);
             } else {
                 float y = 0.f;
-                for (int k = 0; k < G::WK; ++k) y += pt[k * 16 + ct];
-                p.out[u] += y;
+                for (int k = 0; k < G::WK; ++k) y += pt[k * MAX_ROWS + ct];
+                if (MODE == MODE_QMV)
+                    p.out[u] = y;
+                else
+                    p.out[u] += y;
             }
         }
     }

@@ -203,3 +203,25 @@ def test_moe_prefill_workload_sampled(qm, orc):
             assert route_is_valid(idx[t], logits[t], scales[t], K), t
             mismatched += list(idx[t]) != list(ri)
     assert mismatched <= 5
+
+
+# ----------------------------------------------- many tokens (tensor cores)
+MOE_PREFILL_SMALL = [
+    dict(hidden=256, expert_dim=256, num_experts=8, top_k=2, n_tokens=64),
+    dict(hidden=512, expert_dim=512, num_experts=16, top_k=4, n_tokens=40),
+    dict(hidden=256, expert_dim=256, num_experts=2, top_k=1, n_tokens=300),   # >128 per expert
+    dict(hidden=768, expert_dim=256, num_experts=64, top_k=8, n_tokens=32),   # smallest T
+    dict(hidden=256, expert_dim=768, num_experts=33, top_k=3, n_tokens=97),
+]
+
+
+@pytest.mark.parametrize("shp", MOE_PREFILL_SMALL,
+                         ids=lambda s: "H{hidden}F{expert_dim}E{num_experts}k{top_k}T{n_tokens}".format(**s))
+def test_moe_many_tokens_all_checked(qm, orc, shp):
+    """Grouped tensor-core path (Q4_K gate/up, Q6_K down): every token."""
+    shp = dict(shp, gate=synth.Q4_K, up=synth.Q4_K, down=synth.Q6_K)
+    inp = synth.moe_inputs(71 + shp["n_tokens"], **shp)
+    out, idx, w = gpu_moe(qm, inp, shp)
+    ref = oracle_moe(orc, inp, shp)
+    assert check_moe(out, idx, w, ref) <= max(2, shp["n_tokens"] // 20)
+    assert qm.device_status() == qm.OK
