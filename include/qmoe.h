@@ -149,6 +149,34 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
                     float* residual, int32_t* topk_idx, float* topk_w, void* ws,
                     size_t ws_bytes, void* stream);
 
+/* Bytes of the built-in scratch used by moe_ffn_noalloc. */
+#define QMOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* moe_ffn without a caller workspace, for callers that cannot allocate
+ * device memory.  Examples: a runtime where another framework owns all
+ * device memory and hands out none of it, or a serving loop that forbids
+ * allocation once it has started.
+ * The pages have no counterpart of this call; it is an addition of this
+ * library.  Arguments and results are those of moe_ffn, minus ws/ws_bytes.
+ *   - Scratch comes from one QMOE_NOALLOC_SCRATCH_BYTES device array built
+ *     into the library.  Every GPU that loads the library holds that array
+ *     until the process exits.  Nothing is allocated or freed by this call:
+ *     no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Shapes whose moe_ffn_workspace_size exceeds the array are refused with
+ *     QMOE_ERR_UNSUPPORTED and a message giving both sizes.  For a layer of
+ *     hidden 2048, 128 experts, top-8, expert_dim 768 that allows up to 35
+ *     tokens per call; larger batches need moe_ffn and a workspace.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Nothing in it has to start at zero: every call writes what it reads.
+ *     Calls that overlap on the GPU (other streams, other host threads)
+ *     race on it, so order them on one stream or synchronise between them. */
+qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const void* up_stack,
+                            const void* down_stack, const qmoe_moe_shape* shape, const float* x,
+                            float* residual, int32_t* topk_idx, float* topk_w, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QMOE_ERR_TIMEOUT if a bounded device wait expired since the last
  * read, QMOE_ERR_CUDA if the stream reported an error, else QMOE_OK. */

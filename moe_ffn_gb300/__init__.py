@@ -85,6 +85,8 @@ SIGNATURES = {
     "moe_ffn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(_Shape)]),
     "moe_ffn": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(_Shape), _P, _P, _P, _P, _P,
                                ctypes.c_size_t, _P]),
+    "moe_ffn_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(_Shape), _P, _P, _P, _P,
+                                        _P]),
     "qmoe_device_status": (ctypes.c_int, [_P]),
     "qmoe_last_error": (ctypes.c_char_p, []),
     "qmoe_row_bytes": (_I64, [ctypes.c_int, _I64]),
@@ -174,6 +176,20 @@ def moe_ffn(router_W, gate_stack, up_stack, down_stack, shape: _Shape, x, residu
     _check(lib().moe_ffn(_ptr(router_W), _ptr(gate_stack), _ptr(up_stack), _ptr(down_stack),
                          ctypes.byref(shape), _ptr(x), _ptr(residual), _ptr(topk_idx),
                          _ptr(topk_w), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 1 << 20
+
+
+def moe_ffn_noalloc(router_W, gate_stack, up_stack, down_stack, shape: _Shape, x, residual,
+                    topk_idx=None, topk_w=None, stream=None) -> None:
+    """moe_ffn without a workspace argument: for callers that cannot allocate
+    device memory.  Scratch is the library's built-in array
+    (NOALLOC_SCRATCH_BYTES); calls share it, so calls that overlap on the
+    GPU race (see include/qmoe.h)."""
+    _check(lib().moe_ffn_noalloc(_ptr(router_W), _ptr(gate_stack), _ptr(up_stack),
+                                 _ptr(down_stack), ctypes.byref(shape), _ptr(x), _ptr(residual),
+                                 _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
 
 
 def device_status(stream=None) -> int:

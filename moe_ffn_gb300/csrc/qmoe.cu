@@ -620,6 +620,46 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
     return QMOE_OK;
 }
 
+// ----------------------------------------------------- allocation-free call
+// Scratch for moe_ffn_noalloc: a file-scope device array, so the call needs
+// no allocation at all.  Every GPU that loads the library holds it until the
+// process exits.  Host code may not use the symbol's name as a device
+// address: the address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and passed down.
+static __device__ __align__(256) unsigned char g_noalloc_ws[QMOE_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_ptr[64];
+static std::mutex g_noalloc_mu;
+
+qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const void* up_stack,
+                            const void* down_stack, const qmoe_moe_shape* shape, const float* x,
+                            float* residual, int32_t* topk_idx, float* topk_w, void* stream) {
+    g_last_error.clear();
+    if (!shape) return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn_noalloc: null shape");
+    const size_t need = moe_ffn_workspace_size(shape);
+    if (need > QMOE_NOALLOC_SCRATCH_BYTES)
+        return fail(QMOE_ERR_UNSUPPORTED,
+                    "moe_ffn_noalloc: this shape needs %zu bytes of scratch; the built-in "
+                    "scratch holds %zu (use moe_ffn with a workspace)",
+                    need, static_cast<size_t>(QMOE_NOALLOC_SCRATCH_BYTES));
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(QMOE_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+            g_noalloc_ptr[dev] = ptr;
+        }
+        ws = g_noalloc_ptr[dev];
+    }
+    return moe_ffn(router_W, gate_stack, up_stack, down_stack, shape, x, residual, topk_idx,
+                   topk_w, ws, QMOE_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 qmoe_status qmoe_device_status(void* stream) {
     g_last_error.clear();
     DevInfo* d = nullptr;
