@@ -496,6 +496,16 @@ def run_profile_case(case, launches):
         for _ in range(launches):
             qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, d["x"], d["residual"],
                        None, None, ws)
+    elif case == "moe_prefill":
+        shp = synth.MOE_PREFILL
+        inp = synth.moe_inputs(0, **shp)
+        s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"],
+                         shp["n_tokens"], shp["gate"], shp["up"], shp["down"])
+        d = {k: torch.from_numpy(inp[k]).to(dev) for k in inp}
+        ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device=dev)
+        for _ in range(launches):
+            qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, d["x"], d["residual"],
+                       None, None, ws)
     elif case == "ffn":
         w = synth.DENSE_FFN
         fin = synth.ffn_inputs(0, **w)

@@ -34,46 +34,64 @@ namespace pf {
 enum : unsigned { DEV_PF_TIMEOUT = 16, DEV_PF_RANGE = 17 };
 
 // ------------------------------------------------------------------ router
-// One thread per (token, expert): warp = 32 experts of one token.  The sum
-// runs in three levels (16 products, 16 of those, the rest) so its f32 error
-// stays near 40 ulp of sum |R x| whatever H is.
-constexpr int RT_TOK = 8;  // tokens per CTA (one per warp)
+// CTA = 8 tokens x 32 experts (one thread each; a warp is one token).  x and
+// R are staged through shared memory 256 columns at a time (R rows padded to
+// 260 floats so a warp's 32 rows fall in distinct banks).  The sum runs in
+// three levels (16 products, 16 of those, the rest) so its f32 error stays
+// near 40 ulp of sum |R x| whatever H is.
+constexpr int RT_TOK = 8;   // tokens per CTA (one per warp)
+constexpr int RT_KC = 256;  // columns per staged chunk
+constexpr int RT_LD = 260;  // padded row stride (floats)
 
 __global__ void __launch_bounds__(256) pf_router_kernel(const float* __restrict__ R,
                                                         const float* __restrict__ X, int T,
                                                         int H, int E, float* __restrict__ logits,
                                                         int32_t* __restrict__ cnt) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * RT_TOK + warp;
-    const int e = blockIdx.y * 32 + lane;
+    __shared__ __align__(16) float sx[RT_TOK][RT_KC];
+    __shared__ __align__(16) float sr[32][RT_LD];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * RT_TOK, e0 = blockIdx.y * 32;
+    const int t = t0 + warp, e = e0 + lane;
     pdl_wait();
     pdl_trigger();
     if (blockIdx.x == 0 && blockIdx.y == 0)
-        for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
-    if (t >= T) return;
-    const float4* x4 = reinterpret_cast<const float4*>(X + static_cast<int64_t>(t) * H);
-    const float4* r4 = reinterpret_cast<const float4*>(R + static_cast<int64_t>(e < E ? e : 0) * H);
+        for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
     float total = 0.f;
-    for (int k0 = 0; k0 < H / 4; k0 += 64) {  // 256 elements
+    for (int k0 = 0; k0 < H; k0 += RT_KC) {
+        __syncthreads();
+        // stage x[t0..t0+7][k0..k0+255] and R[e0..e0+31][k0..k0+255] (float4s)
+        for (int i = tid; i < RT_TOK * RT_KC / 4; i += 256) {
+            const int r = i / (RT_KC / 4), c4 = i % (RT_KC / 4);
+            const int tt = min(t0 + r, T - 1);
+            reinterpret_cast<float4*>(&sx[r][0])[c4] =
+                __ldcg(reinterpret_cast<const float4*>(X + static_cast<int64_t>(tt) * H + k0) + c4);
+        }
+        for (int i = tid; i < 32 * RT_KC / 4; i += 256) {
+            const int r = i / (RT_KC / 4), c4 = i % (RT_KC / 4);
+            const int ee = min(e0 + r, E - 1);
+            reinterpret_cast<float4*>(&sr[r][0])[c4] =
+                __ldg(reinterpret_cast<const float4*>(R + static_cast<int64_t>(ee) * H + k0) + c4);
+        }
+        __syncthreads();
         float mid = 0.f;
-        for (int k1 = k0; k1 < k0 + 64 && k1 < H / 4; k1 += 4) {  // 16 elements
+        const float4* xr = reinterpret_cast<const float4*>(&sx[warp][0]);
+        const float4* rr = reinterpret_cast<const float4*>(&sr[lane][0]);
+#pragma unroll 4
+        for (int k16 = 0; k16 < RT_KC / 16; ++k16) {
             float lo = 0.f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int kk = k1 + k;
-                if (kk < H / 4) {
-                    const float4 xv = __ldcg(x4 + kk), rv = __ldg(r4 + kk);
-                    lo = fmaf(xv.x, rv.x, lo);
-                    lo = fmaf(xv.y, rv.y, lo);
-                    lo = fmaf(xv.z, rv.z, lo);
-                    lo = fmaf(xv.w, rv.w, lo);
-                }
+                const float4 xv = xr[4 * k16 + k], rv = rr[4 * k16 + k];
+                lo = fmaf(xv.x, rv.x, lo);
+                lo = fmaf(xv.y, rv.y, lo);
+                lo = fmaf(xv.z, rv.z, lo);
+                lo = fmaf(xv.w, rv.w, lo);
             }
             mid += lo;
         }
         total += mid;
     }
-    if (e < E) logits[static_cast<int64_t>(t) * E + e] = total;
+    if (t < T && e < E) logits[static_cast<int64_t>(t) * E + e] = total;
 }
 
 // ------------------------------------------------------------------ top-k
@@ -200,6 +218,15 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Byte k of w as the float 0.5 + w.byte_k / 256, built by one byte permute
+// (the byte lands in the mantissa under exponent 2^-1).  Then
+//   fmaf(f, 256 * s, -(128 * s + c)) = s * byte - c
+// with one rounding; the constant's own rounding is at most 2^-17 * |s|.
+__device__ __forceinline__ float byte_as_half_plus(uint32_t w, uint32_t sel) {
+    return __uint_as_float(__byte_perm(w, 0x3F000000u, sel));
+}
+constexpr uint32_t SEL_B0 = 0x7054, SEL_B1 = 0x7154, SEL_B2 = 0x7254, SEL_B3 = 0x7354;
+
 // f32 -> tf32, round to nearest (ties away), kept in an f32 container.
 __device__ __forceinline__ float to_tf32(float v) {
     uint32_t r;
@@ -215,7 +242,8 @@ constexpr int GU_RAW_ROW = 144;
 constexpr int GU_RAW_STAGE = 256 * GU_RAW_ROW;      // 36,864
 constexpr int GU_TILE = 128 * 128;                  // 16,384 (128 rows x 128 B)
 constexpr int GU_AB_STAGE = 3 * GU_TILE;            // 49,152
-constexpr int GU_SMEM = 1024 + 2 * GU_AB_STAGE + 2 * GU_RAW_STAGE + 256;
+constexpr int PF_META = 96 + 2 * PF_NP * (8 + 4 + 4 + 4);  // barriers + per-pass metadata
+constexpr int GU_SMEM = 1024 + 2 * GU_AB_STAGE + 2 * GU_RAW_STAGE + PF_META;
 
 __global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -231,6 +259,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams
     uint64_t* acc_full = bars + 8;
     uint64_t* acc_empty = bars + 9;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+    int64_t* meta_tok = reinterpret_cast<int64_t*>(bars + 12);          // [2][PF_NP]
+    float* meta_xinv = reinterpret_cast<float*>(meta_tok + 2 * PF_NP);  // [2][PF_NP]
+    float* meta_w = meta_xinv + 2 * PF_NP;                              // [2][PF_NP]
+    int32_t* meta_pair = reinterpret_cast<int32_t*>(meta_w + 2 * PF_NP);  // [2][PF_NP]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int FT = p.F / 128;              // feature tiles per expert
@@ -356,6 +388,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams
         for (int pass = 0; pass < passes; ++pass, ++acc_round) {
             const int nt = min(PF_NP, n - pass * PF_NP);
             const int np = (nt + 15) & ~15;
+            // this pass's tokens: X16 row offset, 1/scale, routing weight, pair
+            int64_t* mt_tok = meta_tok + (acc_round & 1) * PF_NP;
+            float* mt_xinv = meta_xinv + (acc_round & 1) * PF_NP;
+            float* mt_w = meta_w + (acc_round & 1) * PF_NP;
+            int32_t* mt_pair = meta_pair + (acc_round & 1) * PF_NP;
+            if (wt < nt) {
+                const int pair = __ldcg(lst + pass * PF_NP + wt);
+                const int t = pair / p.K;
+                mt_pair[wt] = pair;
+                mt_tok[wt] = static_cast<int64_t>(t) * p.H;
+                mt_xinv[wt] = __ldcg(p.xinv + t);
+                mt_w[wt] = __ldcg(p.tw + pair);
+            }
+            named_bar(2, PF_WORKERS * 32);
             for (int kc = 0; kc < p.H / 64; ++kc, ++kit) {
                 const int s = kit & 1, round = kit >> 1;
                 if (round > 0 &&
@@ -365,16 +411,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams
                 // B: rows j < np (tokens of this pass), 64 f16 of X16 at column kc*64
                 for (int c = wt; c < np * 8; c += 256) {
                     const int j = c >> 3, ch = c & 7;
-                    if (j < nt) {
-                        const int pair = __ldcg(lst + pass * PF_NP + j);
-                        const int t = pair / p.K;
-                        const __half* src = p.X16 + static_cast<int64_t>(t) * p.H + kc * 64 + ch * 8;
-                        cp_async16(st + 2 * GU_TILE + umma::sw128_offset(j, ch * 16), src);
-                    } else {
-                        *reinterpret_cast<uint4*>(st + 2 * GU_TILE +
-                                                  umma::sw128_offset(j, ch * 16)) =
-                            make_uint4(0, 0, 0, 0);
-                    }
+                    uint8_t* dst = st + 2 * GU_TILE + umma::sw128_offset(j, ch * 16);
+                    if (j < nt)
+                        cp_async16(dst, p.X16 + mt_tok[j] + kc * 64 + ch * 8);
+                    else
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
                 }
                 // A: thread wt decodes quarter (kc % 4) of super-block kc/4 of row wt
                 const int qtr = kc & 3;
@@ -391,37 +432,51 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams
                     float sca, ma, scb, mb;
                     FmtQ4K::scale_min(hd.y, hd.z, hd.w, qtr, sca, ma, scb, mb);
                     const float d1 = d * sca, m1 = dmin * ma, d2 = d * scb, m2 = dmin * mb;
+                    // largest |value| of either half: 15|d*sc| + |dmin*m|
+                    const float bound = fmaxf(fmaf(15.f, fabsf(d1), fabsf(m1)),
+                                              fmaf(15.f, fabsf(d2), fabsf(m2)));
+                    if (bound > 65504.f && bound < INFINITY) atomicCAS(p.err, 0u, DEV_PF_RANGE);
+                    const float A1 = 256.f * d1, C1 = -fmaf(128.f, d1, m1);
+                    const float A2 = 256.f * d2, C2 = -fmaf(128.f, d2, m2);
                     const uint4 q0 = *reinterpret_cast<const uint4*>(sb + 16 + 32 * qtr);
                     const uint4 q1 = *reinterpret_cast<const uint4*>(sb + 16 + 32 * qtr + 16);
                     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    // element 64*qtr + l (low nibble of byte l) and +32 (high nibble)
+                    // element 64*qtr + l: low nibble of byte l; +32: high nibble
                     uint8_t* arow = st + (wt < 128 ? 0 : GU_TILE);
                     const int r = wt & 127;
-                    float rng = 0.f;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {       // low nibbles, then high
-                        const float dd = hh ? d2 : d1, mm = hh ? m2 : m1;
+                    for (int c = 0; c < 4; ++c) {      // bytes l = 8c .. 8c+7
+                        uint32_t lo[2], hi[2];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {      // 16-byte chunks: 8 values
-                            uint32_t h2[4];
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const uint32_t w = qw[2 * c + (v >> 1)];
-                                const int sh = 16 * (v & 1) + 4 * hh;
-                                const float a0 = fmaf(dd, static_cast<float>((w >> sh) & 15u), -mm);
-                                const float a1 =
-                                    fmaf(dd, static_cast<float>((w >> (sh + 8)) & 15u), -mm);
-                                rng = fmaxf(rng, fmaxf(fabsf(a0), fabsf(a1)));
-                                const __half2 hv = __floats2half2_rn(a0, a1);
-                                h2[v] = *reinterpret_cast<const uint32_t*>(&hv);
-                            }
-                            // values l = 8c..8c+7 of this half; column 32*hh + 8c
-                            const int col = 32 * hh + 8 * c;
-                            *reinterpret_cast<uint4*>(arow + umma::sw128_offset(r, col * 2)) =
-                                make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                        for (int k = 0; k < 2; ++k) {
+                            lo[k] = qw[2 * c + k] & 0x0F0F0F0Fu;
+                            hi[k] = (qw[2 * c + k] >> 4) & 0x0F0F0F0Fu;
                         }
+                        uint32_t hl[4], hh[4];
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const __half2 a01 = __floats2half2_rn(
+                                fmaf(byte_as_half_plus(lo[k], SEL_B0), A1, C1),
+                                fmaf(byte_as_half_plus(lo[k], SEL_B1), A1, C1));
+                            const __half2 a23 = __floats2half2_rn(
+                                fmaf(byte_as_half_plus(lo[k], SEL_B2), A1, C1),
+                                fmaf(byte_as_half_plus(lo[k], SEL_B3), A1, C1));
+                            const __half2 b01 = __floats2half2_rn(
+                                fmaf(byte_as_half_plus(hi[k], SEL_B0), A2, C2),
+                                fmaf(byte_as_half_plus(hi[k], SEL_B1), A2, C2));
+                            const __half2 b23 = __floats2half2_rn(
+                                fmaf(byte_as_half_plus(hi[k], SEL_B2), A2, C2),
+                                fmaf(byte_as_half_plus(hi[k], SEL_B3), A2, C2));
+                            hl[2 * k] = *reinterpret_cast<const uint32_t*>(&a01);
+                            hl[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&a23);
+                            hh[2 * k] = *reinterpret_cast<const uint32_t*>(&b01);
+                            hh[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b23);
+                        }
+                        *reinterpret_cast<uint4*>(arow + umma::sw128_offset(r, (8 * c) * 2)) =
+                            make_uint4(hl[0], hl[1], hl[2], hl[3]);
+                        *reinterpret_cast<uint4*>(arow + umma::sw128_offset(r, (32 + 8 * c) * 2)) =
+                            make_uint4(hh[0], hh[1], hh[2], hh[3]);
                     }
-                    if (rng > 65504.f && rng < INFINITY) atomicCAS(p.err, 0u, DEV_PF_RANGE);
                 }
                 if (qtr == 3) {
                     __syncwarp();
@@ -449,12 +504,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams
                 for (int i = 0; i < 16; ++i) {
                     const int j = cb + i;
                     if (j < nt && j < c1) {
-                        const int pair = __ldcg(lst + pass * PF_NP + j);
-                        const int t = pair / p.K;
-                        const float xi = __ldcg(p.xinv + t);
+                        const float xi = mt_xinv[j];
                         const float gv = g[i] * xi, uv = u[i] * xi;
-                        p.a[static_cast<int64_t>(pair) * p.F + f] =
-                            __ldcg(p.tw + pair) * ((gv / (1.0f + expf(-gv))) * uv);
+                        p.a[static_cast<int64_t>(mt_pair[j]) * p.F + f] =
+                            mt_w[j] * ((gv / (1.0f + expf(-gv))) * uv);
                     }
                 }
             }
@@ -479,7 +532,7 @@ constexpr int DN_RAW_ROW = 240;
 constexpr int DN_RAW_STAGE = 128 * DN_RAW_ROW;      // 30,720
 constexpr int DN_TILE = 128 * 128;                  // 16,384
 constexpr int DN_AB_STAGE = 2 * DN_TILE;            // 32,768
-constexpr int DN_SMEM = 1024 + 2 * DN_AB_STAGE + 2 * DN_RAW_STAGE + 256;
+constexpr int DN_SMEM = 1024 + 2 * DN_AB_STAGE + 2 * DN_RAW_STAGE + PF_META;
 
 __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -495,6 +548,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
     uint64_t* acc_full = bars + 8;
     uint64_t* acc_empty = bars + 9;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+    int64_t* meta_res = reinterpret_cast<int64_t*>(bars + 12);   // [2][PF_NP] residual row offset
+    int64_t* meta_act = meta_res + 2 * PF_NP;                    // [2][PF_NP] activation row offset
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int MT = p.H / 128;              // row tiles per expert
@@ -626,26 +681,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
         for (int pass = 0; pass < passes; ++pass, ++acc_round) {
             const int nt = min(PF_NP, n - pass * PF_NP);
             const int np = (nt + 15) & ~15;
+            int64_t* mt_res = meta_res + (acc_round & 1) * PF_NP;
+            int64_t* mt_act = meta_act + (acc_round & 1) * PF_NP;
+            if (wt < nt) {
+                const int pair = __ldcg(lst + pass * PF_NP + wt);
+                mt_res[wt] = static_cast<int64_t>(pair / p.K) * p.H;
+                mt_act[wt] = static_cast<int64_t>(pair) * p.F;
+            }
+            named_bar(2, PF_WORKERS * 32);
             for (int kc = 0; kc < p.F / 32; ++kc, ++kit) {
                 const int s = kit & 1, round = kit >> 1;
                 if (round > 0 &&
                     !mbar_wait_bounded(&ab_empty[s], (round - 1) & 1, p.err, DEV_PF_TIMEOUT))
                     goto done;
                 uint8_t* st = ab + s * DN_AB_STAGE;
-                // B: activations a[pair][kc*32 .. +32] rounded to tf32
-                for (int c = wt; c < np * 8; c += 256) {
-                    const int j = c >> 3, ch = c & 7;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (j < nt) {
-                        const int pair = __ldcg(lst + pass * PF_NP + j);
-                        v = __ldcg(reinterpret_cast<const float4*>(
-                            p.a + static_cast<int64_t>(pair) * p.F + kc * 32 + ch * 4));
-                        v.x = to_tf32(v.x);
-                        v.y = to_tf32(v.y);
-                        v.z = to_tf32(v.z);
-                        v.w = to_tf32(v.w);
-                    }
-                    *reinterpret_cast<float4*>(st + DN_TILE + umma::sw128_offset(j, ch * 16)) = v;
+                // B: activations a[pair][kc*32 .. +32]; loads issued now, rounded
+                // to tf32 and stored after the A decode below
+                float4 bv[PF_NP * 8 / 256];
+#pragma unroll
+                for (int k = 0; k < PF_NP * 8 / 256; ++k) {
+                    const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
+                    bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (j < nt)
+                        bv[k] = __ldcg(reinterpret_cast<const float4*>(p.a + mt_act[j] + kc * 32 +
+                                                                       ch * 4));
                 }
                 // A: row r = wt/2, 16 values (half hh) of the 32-element chunk
                 const int sbk = kc & 7;            // chunk within the super-block
@@ -674,24 +733,35 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
                     const uint32_t sw = *reinterpret_cast<const uint32_t*>(sa & ~uintptr_t(3));
                     const float scl = static_cast<float>(static_cast<int8_t>(sw >> ((sa & 3u) * 8u)));
                     const float ds = d * scl;
-                    float vals[16];
+                    const float A = 256.f * ds, C = -160.f * ds;   // value = ds * (q6 - 32)
+                    uint32_t v[4];
 #pragma unroll
                     for (int wv = 0; wv < 4; ++wv) {
-#pragma unroll
-                        for (int bb = 0; bb < 4; ++bb) {
-                            const uint32_t lo4 = (QL[wv] >> (8 * bb + 4 * (t >> 1))) & 15u;
-                            const uint32_t hi2 = (QH[wv] >> (8 * bb + 2 * t)) & 3u;
-                            const int q = static_cast<int>(lo4 | (hi2 << 4)) - 32;
-                            vals[4 * wv + bb] = to_tf32(ds * static_cast<float>(q));
-                        }
+                        const uint32_t lo4 = (QL[wv] >> (4 * (t >> 1))) & 0x0F0F0F0Fu;
+                        const uint32_t hi2 = ((QH[wv] >> (2 * t)) & 0x03030303u) << 4;
+                        v[wv] = lo4 | hi2;                      // four 6-bit values, one per byte
                     }
                     uint8_t* arow = st;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int col = 16 * hh + 4 * c;   // tf32 column in the 32-wide chunk
                         *reinterpret_cast<float4*>(arow + umma::sw128_offset(r, col * 4)) =
-                            make_float4(vals[4 * c], vals[4 * c + 1], vals[4 * c + 2],
-                                        vals[4 * c + 3]);
+                            make_float4(to_tf32(fmaf(byte_as_half_plus(v[c], SEL_B0), A, C)),
+                                        to_tf32(fmaf(byte_as_half_plus(v[c], SEL_B1), A, C)),
+                                        to_tf32(fmaf(byte_as_half_plus(v[c], SEL_B2), A, C)),
+                                        to_tf32(fmaf(byte_as_half_plus(v[c], SEL_B3), A, C)));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < PF_NP * 8 / 256; ++k) {
+                    const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
+                    if (j < np) {
+                        float4 w = bv[k];
+                        w.x = to_tf32(w.x);
+                        w.y = to_tf32(w.y);
+                        w.z = to_tf32(w.z);
+                        w.w = to_tf32(w.w);
+                        *reinterpret_cast<float4*>(st + DN_TILE + umma::sw128_offset(j, ch * 16)) = w;
                     }
                 }
                 if (sbk == 7) {
@@ -717,11 +787,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int j = cb + k;
-                    if (j < nt && j < c1) {
-                        const int pair = __ldcg(lst + pass * PF_NP + j);
-                        const int t = pair / p.K;
-                        atomicAdd(p.residual + static_cast<int64_t>(t) * p.H + i, dv[k]);
-                    }
+                    if (j < nt && j < c1) atomicAdd(p.residual + mt_res[j] + i, dv[k]);
                 }
             }
             umma::fence_before_sync();
