@@ -287,13 +287,26 @@ def time_replays(torch, g, replays):
     return e0.elapsed_time(e1)
 
 
+GEMV_SOURCES = ("formats.cuh", "ptx.cuh", "stream.cuh")
+
+
+def gemv_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMV_SOURCES:
+        with open(os.path.join(ROOT, "moe_ffn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(key):
-    """dram bytes per launch from the committed ncu summary, if current."""
+    """dram bytes per launch from the committed ncu summary, or None if the
+    kernel's sources changed since that capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(p):
         d = json.load(open(p))
         v = d.get(key)
-        if isinstance(v, dict):
+        if isinstance(v, dict) and v.get("src_sha256_16") == gemv_source_hash():
             return v.get("bytes_per_launch")
     return None
 

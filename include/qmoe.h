@@ -179,7 +179,9 @@ qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QMOE_ERR_TIMEOUT if a bounded device wait expired since the last
- * read, QMOE_ERR_CUDA if the stream reported an error, else QMOE_OK. */
+ * read; QMOE_ERR_UNSUPPORTED if the many-token MoE path met a decoded gate/up
+ * weight outside f16 range (its output is then not valid); QMOE_ERR_CUDA if
+ * the stream reported an error; else QMOE_OK. */
 qmoe_status qmoe_device_status(void* stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */

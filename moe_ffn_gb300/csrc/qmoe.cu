@@ -672,8 +672,14 @@ qmoe_status qmoe_device_status(void* stream) {
     if (v) {
         e = cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        if (v == pf::DEV_PF_RANGE)
+            return fail(QMOE_ERR_UNSUPPORTED,
+                        "a decoded gate/up weight is outside f16 range (code %u); the "
+                        "many-token path cannot represent it", v);
         return fail(QMOE_ERR_TIMEOUT, "a bounded device wait expired (code %u: %s)", v,
-                    v == DEV_TIMEOUT_FULL ? "stage never filled" : "stage never released");
+                    v == DEV_TIMEOUT_FULL    ? "stage never filled"
+                    : v == DEV_TIMEOUT_EMPTY ? "stage never released"
+                                             : "tensor-core pipeline stalled");
     }
     return QMOE_OK;
 }

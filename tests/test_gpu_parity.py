@@ -225,3 +225,21 @@ def test_moe_many_tokens_all_checked(qm, orc, shp):
     ref = oracle_moe(orc, inp, shp)
     assert check_moe(out, idx, w, ref) <= max(2, shp["n_tokens"] // 20)
     assert qm.device_status() == qm.OK
+
+
+def test_moe_many_tokens_f16_range_reported(qm):
+    """A Q4_K gate weight beyond f16 range (d = 60000, scales 63, quants 15)
+    cannot be a tensor-core operand: the many-token path reports it as
+    UNSUPPORTED through the device status, and the status is cleared after."""
+    shp = dict(hidden=256, expert_dim=256, num_experts=4, top_k=2, n_tokens=64,
+               gate=synth.Q4_K, up=synth.Q4_K, down=synth.Q6_K)
+    inp = synth.moe_inputs(9, **shp)
+    gate = inp["gate"].reshape(shp["num_experts"], shp["expert_dim"], -1).copy()
+    blocks = gate.reshape(shp["num_experts"], shp["expert_dim"], -1, 144)
+    blocks[:, 0, :, 0:2] = np.frombuffer(np.float16(60000.0).tobytes(), np.uint8)
+    blocks[:, 0, :, 4:] = 0xFF
+    inp["gate"] = gate.reshape(inp["gate"].shape)
+    gpu_moe(qm, inp, shp)
+    assert qm.device_status() == qm.ERR_UNSUPPORTED
+    assert "f16 range" in qm.last_error()
+    assert qm.device_status() == qm.OK
