@@ -103,7 +103,8 @@ typedef struct {
 qmoe_status qmv(int qtype, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
                 void* stream);
 
-/* Bytes of workspace ffn_swiglu needs: inter f32 activations. */
+/* Bytes of workspace ffn_swiglu needs: 256 bytes of grid-barrier state plus
+ * inter f32 activations. */
 size_t ffn_swiglu_workspace_size(int64_t hidden, int64_t inter);
 
 /* residual += down( silu(gate x) * (up x) ) — launch_dense_ffn_swiglu on
@@ -116,14 +117,23 @@ size_t ffn_swiglu_workspace_size(int64_t hidden, int64_t inter);
  *   x          [hidden] f32, the FFN input (after the norm)
  *   residual   [hidden] f32, updated in place
  *   ws         >= ffn_swiglu_workspace_size bytes of device memory, 16-byte
- *              aligned; its contents are scratch
+ *              aligned; its contents are scratch (it may hold anything before
+ *              a call); calls that overlap on the GPU must not share one
  * Shape rules of apply_gpu_dense_ffn_swiglu (gate.cols == up.cols == x.len,
- * down.cols == gate.rows) hold by construction of the arguments. */
+ * down.cols == gate.rows) hold by construction of the arguments.
+ * The layer runs as one cooperative kernel (one CTA per SM): the gate/up
+ * rows and then the down rows stream through one pipeline, and a grid
+ * barrier orders the activations between the two products.  A layer that does
+ * not fit that kernel's shared memory runs as two kernels instead.  Setting
+ * the environment variable QMOE_FUSED=0 (read once per process) forces the
+ * two-kernel form, for diagnostics. */
 qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int gate_qtype,
                        int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
                        const float* x, float* residual, void* ws, size_t ws_bytes, void* stream);
 
-/* Bytes of workspace moe_ffn needs for this shape. */
+/* Bytes of workspace moe_ffn needs for this shape (256 bytes of grid-barrier
+ * state, then the logits, activations and, for many tokens, the grouping
+ * buffers). */
 size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
 
 /* The MoE FFN of one layer for T tokens — moe_layer on "aprender-serve
@@ -140,7 +150,16 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  *   x           [T][H] f32 (normed input);  residual [T][H] f32, in place
  *   topk_idx    [T][k] int32 or NULL: routed experts in rank order
  *   topk_w      [T][k] f32 or NULL: their renormalised weights
- *   ws          >= moe_ffn_workspace_size(shape) bytes, 16-byte aligned; scratch
+ *   ws          >= moe_ffn_workspace_size(shape) bytes, 16-byte aligned;
+ *               scratch that may hold anything before a call; calls that
+ *               overlap on the GPU must not share one
+ * Execution: for T >= 32 tokens with Q4_K gate/up and Q6_K down stacks, the
+ * tokens are grouped by expert and the expert products run on the tensor
+ * cores.  Otherwise each token runs one cooperative kernel (one CTA per SM):
+ * router GEMV, a grid barrier, routing in every CTA, the routed gate/up rows
+ * and then the down rows streamed through one pipeline, a second grid barrier
+ * before the down products.  QMOE_FUSED=0 (see ffn_swiglu) replaces that
+ * kernel by three launches per token.
  * Errors: INVALID_ARGUMENT (null, shape fields out of range, k > E, small
  * workspace, misalignment), UNSUPPORTED (E > 256, k > 16, F32 or mixed
  * gate/up formats, sizes not multiples of 256), CUDA. */
@@ -170,7 +189,9 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
  *     (cudaGetSymbolAddress, with that device current); make that first
  *     call before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents.
- *     Nothing in it has to start at zero: every call writes what it reads.
+ *     Nothing in it has to start at zero: every call writes what it reads,
+ *     and the grid-barrier state at its start is checked and reset by the
+ *     kernel itself.
  *     Calls that overlap on the GPU (other streams, other host threads)
  *     race on it, so order them on one stream or synchronise between them. */
 qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const void* up_stack,
@@ -179,7 +200,7 @@ qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QMOE_ERR_TIMEOUT if a bounded device wait expired since the last
- * read; QMOE_ERR_UNSUPPORTED if the many-token MoE path met a decoded gate/up
+ * read (a pipeline stage, or a grid barrier that not every CTA reached); QMOE_ERR_UNSUPPORTED if the many-token MoE path met a decoded gate/up
  * weight outside f16 range (its output is then not valid); QMOE_ERR_CUDA if
  * the stream reported an error; else QMOE_OK. */
 qmoe_status qmoe_device_status(void* stream);

@@ -117,9 +117,18 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
 // nibbles come from the multiply pipe (top_field, __umulhi): both at bit 0.
 struct FmtQ4K {
     static constexpr int SBB = 144;
+    // Row slot stride wanted modulo 128 bytes (-1: any odd multiple of 16)
+    static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) {
         int t = i >> 3, j = i & 7;
         return j < 4 ? 64 * q + 4 * t + j : 64 * q + 32 + 4 * t + (j - 4);
+    }
+    // Inverse of elem on float4 granules: the x' slot (4*i4 + q) holding
+    // elements 4*e4 .. 4*e4+3 of the group.
+    __host__ __device__ static int xslot(int e4) {
+        const int q = e4 >> 4, r4 = e4 & 15;
+        const int i4 = r4 < 8 ? 2 * r4 : 2 * (r4 - 8) + 1;
+        return 4 * i4 + q;
     }
     __host__ __device__ static int pos(int, int i) {
         // bit offsets {0, 8, 16, 0, 4, 12, 20, 0} by i % 8, one byte each
@@ -196,7 +205,9 @@ struct FmtQ4K {
 // field from the multiply pipe -> 0.
 struct FmtQ5K {
     static constexpr int SBB = 176;
+    static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) { return FmtQ4K::elem(q, i); }
+    __host__ __device__ static int xslot(int e4) { return FmtQ4K::xslot(e4); }
     __host__ __device__ static int pos(int, int i) {
         // bit offsets {0, 8, 16, 0} by i % 4
         return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
@@ -264,33 +275,95 @@ struct FmtQ5K {
 // positions (0, 8, 16, 0) (byte 3's field from the multiply pipe).
 struct FmtQ6K {
     static constexpr int SBB = 210;
+    // 32 mod 128: the aligned loads of two row groups in a quarter-warp
+    // fall in disjoint 16-byte bank groups
+    static constexpr int SLOT_REM128 = 32;
     __host__ __device__ static int elem(int q, int i) {
         int u = i >> 4, t = (i >> 2) & 3, j = i & 3;
         return 128 * (q >> 1) + 32 * t + 16 * (q & 1) + 4 * u + j;
     }
+    __host__ __device__ static int xslot(int e4) {
+        const int h = e4 >> 5, t = (e4 >> 3) & 3, c = (e4 >> 2) & 1, u = e4 & 3;
+        return 4 * (4 * u + t) + 2 * h + c;
+    }
     __host__ __device__ static int pos(int, int i) {
         // bit offsets {0, 8, 16, 0} by i % 4
         return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
+    }
+    // Words [4k, 4k+4) of the 32-byte window (lo, hi), J words plus sh bits in.
+    template <int J>
+    __device__ __forceinline__ static void window4(const uint4& lo, const uint4& hi, uint32_t sh,
+                                                   uint32_t (&w)[4]) {
+        const uint32_t r[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(r[J + k], r[J + k + 1], sh);
+    }
+    // Loads of R super-blocks that all sit at byte phase 4J + sh/8 of a
+    // 16-byte granule: aligned 128-bit loads (conflict-free for the slot
+    // strides the planner picks) and funnel shifts.  The tail window reads
+    // up to 14 bytes past the super-block, inside the stage's slack.
+    template <int J, int R>
+    __device__ __forceinline__ static void load_phase(const uint8_t* const (&sb)[R], int h, int c,
+                                                      uint32_t sh, uint32_t (&A)[R][4],
+                                                      uint32_t (&B)[R][4], uint32_t (&H)[R][4],
+                                                      uint32_t (&S)[R][2], uint32_t (&db)[R]) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint4* p = reinterpret_cast<const uint4*>(sb[r] - (4 * J + (sh >> 3)));
+            const int oa = 4 * h + c, oh = 8 + 2 * h + c;
+            window4<J>(p[oa], p[oa + 1], sh, A[r]);
+            window4<J>(p[oa + 2], p[oa + 3], sh, B[r]);
+            window4<J>(p[oh], p[oh + 1], sh, H[r]);
+            const uint4 t1 = p[13];
+            uint32_t T[4];
+            window4<J>(p[12], t1, sh, T);  // sc[0..15]
+            S[r][0] = h ? T[2] : T[0];
+            S[r][1] = h ? T[3] : T[1];
+            const uint32_t tw[4] = {t1.x, t1.y, t1.z, t1.w};
+            db[r] = tw[J] >> sh;
+        }
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float (&x)[64], const float* xs16,
                                                 float (&acc)[R]) {
         const int h = q >> 1, c = q & 1;
-        uint32_t A[R][4], B[R][4], H[R][4];
+        uint32_t A[R][4], B[R][4], H[R][4], S[R][2], db[R];
         float sc[R][4], d[R];
+        // fast path when every row of every lane has the same 16-byte phase
+        const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(sb[0])) & 15u;
+        bool same = ph == static_cast<uint32_t>(__shfl_sync(0xffffffffu, static_cast<int>(ph), 0));
+#pragma unroll
+        for (int r = 1; r < R; ++r)
+            same = same && ((static_cast<uint32_t>(reinterpret_cast<uintptr_t>(sb[r])) & 15u) == ph);
+        if (__all_sync(0xffffffffu, same)) {
+            const uint32_t sh = (ph & 3u) * 8u;
+            switch (ph >> 2) {
+            case 0: load_phase<0, R>(sb, h, c, sh, A, B, H, S, db); break;
+            case 1: load_phase<1, R>(sb, h, c, sh, A, B, H, S, db); break;
+            case 2: load_phase<2, R>(sb, h, c, sh, A, B, H, S, db); break;
+            default: load_phase<3, R>(sb, h, c, sh, A, B, H, S, db); break;
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                load4_u16al(sb[r] + 64 * h + 16 * c, A[r]);
+                load4_u16al(sb[r] + 64 * h + 32 + 16 * c, B[r]);
+                load4_u16al(sb[r] + 128 + 32 * h + 16 * c, H[r]);
+                uint32_t T[4];
+                load4_u16al(sb[r] + 192, T);  // sc[0..15]
+                S[r][0] = h ? T[2] : T[0];
+                S[r][1] = h ? T[3] : T[1];
+                const uintptr_t a = reinterpret_cast<uintptr_t>(sb[r] + 208);
+                const uint32_t dw = *reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+                db[r] = dw >> ((a & 3u) * 8u);
+            }
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            load4_u16al(sb[r] + 64 * h + 16 * c, A[r]);
-            load4_u16al(sb[r] + 64 * h + 32 + 16 * c, B[r]);
-            load4_u16al(sb[r] + 128 + 32 * h + 16 * c, H[r]);
-            uint32_t S[4];
-            load4_u16al(sb[r] + 192, S);  // sc[0..15]
-            const uintptr_t a = reinterpret_cast<uintptr_t>(sb[r] + 208);
-            const uint32_t dw = *reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-            d[r] = f16_bits_to_f32(dw >> ((a & 3u) * 8u));
-            // scales sc[8h + c + 2t], t = 0..3: bytes of S[2h], S[2h+1]
-            const uint32_t s_lo = S[2 * h], s_hi = S[2 * h + 1];
+            d[r] = f16_bits_to_f32(db[r]);
+            // scales sc[8h + c + 2t], t = 0..3: bytes of words 2h, 2h+1 of sc
+            const uint32_t s_lo = S[r][0], s_hi = S[r][1];
             sc[r][0] = static_cast<float>(static_cast<int8_t>(s_lo >> (8 * c)));
             sc[r][1] = static_cast<float>(static_cast<int8_t>(s_lo >> (8 * c + 16)));
             sc[r][2] = static_cast<float>(static_cast<int8_t>(s_hi >> (8 * c)));
@@ -342,7 +415,9 @@ struct FmtQ6K {
 // positions (0, 8, 16, 0).
 struct FmtQ80 {
     static constexpr int SBB = 272;
+    static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) { return 64 * q + i; }
+    __host__ __device__ static int xslot(int e4) { return 4 * (e4 & 15) + (e4 >> 4); }
     __host__ __device__ static int pos(int, int i) {
         // bit offsets {0, 8, 16, 0} by i % 4
         return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
@@ -397,10 +472,16 @@ struct FmtQ80 {
 // j>=4 -> element 32(2q+k) + 16 + 4t + (j-4); positions as Q4_K.
 struct FmtQ40 {
     static constexpr int SBB = 144;
+    static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) {
         int k = i >> 5, t = (i >> 3) & 3, j = i & 7;
         int base = 32 * (2 * q + k);
         return j < 4 ? base + 4 * t + j : base + 16 + 4 * t + (j - 4);
+    }
+    __host__ __device__ static int xslot(int e4) {
+        const int blk = e4 >> 3, r = e4 & 7;  // blk = 2q + k
+        const int i4 = 8 * (blk & 1) + 2 * (r & 3) + (r >= 4 ? 1 : 0);
+        return 4 * i4 + (blk >> 1);
     }
     __host__ __device__ static int pos(int q, int i) { return FmtQ4K::pos(q, i); }
     template <int R>

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -13,6 +14,7 @@
 #include "formats.cuh"
 #include "ptx.cuh"
 #include "stream.cuh"
+#include "fused.cuh"
 #include "prefill.cuh"
 
 namespace qmoe {
@@ -76,6 +78,9 @@ static const char* qname(int qt) {
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int64_t MAX_K = 32768;
+// Every workspace starts with the fused kernel's grid-barrier counters,
+// which each call leaves at zero; the other regions follow.
+constexpr size_t WS_SYNC_BYTES = 256;
 
 // ------------------------------------------------------------ device info
 struct DevInfo {
@@ -139,17 +144,12 @@ static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cud
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Plan chunking and pipeline depth for a streamed GEMV; false if it cannot
-// fit in shared memory.
+// Chunk geometry of a streamed phase for a stage budget (bytes): how rows
+// are cut into chunks, the slot strides and the bytes one stage needs.
+// False if not even one group per row fits.
 template <class Fmt, int MODE>
-static bool plan(StreamParams& p, int smem_optin, int* smem_bytes) {
+static bool plan_chunks(StreamParams& p, int budget) {
     using G = ModeGeom<MODE>;
-    // stage budget: at most 96 KB, and at least two stages must fit beside
-    // the x' table
-    p.stage_bytes = 0;
-    p.nstages = 0;
-    const int room = smem_optin - smem_layout(p).total;
-    int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
     if (budget < G::ROWS * (Fmt::SBB + 31)) return false;
     const int seg_full = p.nb_seg * Fmt::SBB;
     const int piece_full = align_up(seg_full + 15, 16);
@@ -175,9 +175,26 @@ static bool plan(StreamParams& p, int smem_optin, int* smem_bytes) {
     }
     p.piece_stride = align_up(nbp_max * Fmt::SBB + 15, 16);
     p.slot_stride = p.chunk_ks * p.piece_stride;
-    if (p.slot_stride % 32 == 0) p.slot_stride += 16;  // alternate rows across bank halves
+    if (Fmt::SLOT_REM128 >= 0)
+        p.slot_stride += (Fmt::SLOT_REM128 - p.slot_stride % 128 + 128) % 128;
+    else if (p.slot_stride % 32 == 0)
+        p.slot_stride += 16;  // alternate rows across bank halves
     p.stage_bytes = G::ROWS * p.slot_stride;
     p.n_chunk = (p.n_sbc == 1) ? (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks : p.n_kseg * p.n_sbc;
+    return true;
+}
+
+// Plan chunking and pipeline depth for a streamed GEMV; false if it cannot
+// fit in shared memory.
+template <class Fmt, int MODE>
+static bool plan(StreamParams& p, int smem_optin, int* smem_bytes) {
+    // stage budget: at most 96 KB, and at least two stages must fit beside
+    // the x' table
+    p.stage_bytes = 0;
+    p.nstages = 0;
+    const int room = smem_optin - smem_layout(p).total;
+    const int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
+    if (!plan_chunks<Fmt, MODE>(p, budget)) return false;
     p.nstages = 0;
     const int fixed = smem_layout(p).total;
     int ns = (smem_optin - fixed) / p.stage_bytes;
@@ -221,6 +238,115 @@ static qmoe_status dispatch(int qt, const StreamParams& p, const DevInfo& d, cud
     case QT_Q5_K: return run_stream<FmtQ5K, MODE>(p, d, st);
     case QT_Q6_K: return run_stream<FmtQ6K, MODE>(p, d, st);
     default: return fail(QMOE_ERR_UNSUPPORTED, "qtype %d has no streamed GEMV", qt);
+    }
+}
+
+// ------------------------------------------------------- fused FFN layer
+// Plan both phases of the fused kernel with one stage size; false if the
+// layer does not fit (then the caller runs the phases as separate kernels).
+template <class FmtG, class FmtD>
+static bool plan_fused(FusedParams& f, int smem_optin, int* smem_bytes) {
+    f.gu.stage_bytes = f.dn.stage_bytes = 0;
+    f.gu.nstages = f.dn.nstages = 0;
+    const int room = smem_optin - fused_layout(f).total;
+    const int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
+    if (!plan_chunks<FmtG, MODE_GATEUP>(f.gu, budget)) return false;
+    if (!plan_chunks<FmtD, MODE_DOWN>(f.dn, budget)) return false;
+    const int sb = f.gu.stage_bytes > f.dn.stage_bytes ? f.gu.stage_bytes : f.dn.stage_bytes;
+    int ns = room / sb;
+    if (ns > MAX_STAGES) ns = MAX_STAGES;
+    if (ns < 2) return false;
+    f.gu.stage_bytes = f.dn.stage_bytes = sb;
+    f.gu.nstages = f.dn.nstages = ns;
+    *smem_bytes = fused_layout(f).total;
+    return *smem_bytes <= smem_optin;
+}
+
+// Whether cooperative launches may also carry programmatic stream
+// serialisation on this driver (probed on first use, per process).
+static int g_coop_pdl = -1;
+
+// 1: launched; 0: the layer does not fit the fused kernel (nothing
+// launched); negative: a CUDA error (status in *err).
+template <class FmtG, class FmtD>
+static int run_fused(FusedParams f, const DevInfo& d, cudaStream_t st, qmoe_status* err) {
+    int smem = 0;
+    if (!plan_fused<FmtG, FmtD>(f, d.smem_optin, &smem)) return 0;
+    auto kern = fused_ffn_kernel<FmtG, FmtD>;
+    static int configured_smem[64] = {};  // per instantiation and device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (smem > configured_smem[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) {
+            *err = cuda_fail(e, "cudaFuncSetAttribute (fused)");
+            return -1;
+        }
+        configured_smem[dev & 63] = smem;
+    }
+    f.err = f.gu.err = f.dn.err = d.err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(d.sms));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_coop_pdl == 0 ? 1 : 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, f);
+    if (e != cudaSuccess && g_coop_pdl < 0) {
+        // if the driver rejects the pair, run without programmatic serialisation
+        (void)cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, f);
+        if (e == cudaSuccess) g_coop_pdl = 0;
+    }
+    if (e != cudaSuccess) {
+        *err = cuda_fail(e, "fused FFN launch");
+        return -1;
+    }
+    if (g_coop_pdl < 0) g_coop_pdl = 1;
+    return 1;
+}
+
+template <class FmtG>
+static int dispatch_fused_d(int dq, const FusedParams& f, const DevInfo& d, cudaStream_t st,
+                            qmoe_status* err) {
+    switch (dq) {
+    case QT_Q8_0: return run_fused<FmtG, FmtQ80>(f, d, st, err);
+    case QT_Q4_0: return run_fused<FmtG, FmtQ40>(f, d, st, err);
+    case QT_Q4_K: return run_fused<FmtG, FmtQ4K>(f, d, st, err);
+    case QT_Q5_K: return run_fused<FmtG, FmtQ5K>(f, d, st, err);
+    case QT_Q6_K: return run_fused<FmtG, FmtQ6K>(f, d, st, err);
+    default: return 0;
+    }
+}
+
+// Fused layer for these formats: 1 launched, 0 not applicable (the caller
+// runs separate kernels), negative on a CUDA error.  The fused kernel can be
+// switched off with the environment variable QMOE_FUSED=0 (diagnostics).
+static bool fused_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("QMOE_FUSED");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+static int dispatch_fused(int gq, int dq, const FusedParams& f, const DevInfo& d, cudaStream_t st,
+                          qmoe_status* err) {
+    if (!fused_enabled()) return 0;
+    switch (gq) {
+    case QT_Q8_0: return dispatch_fused_d<FmtQ80>(dq, f, d, st, err);
+    case QT_Q4_0: return dispatch_fused_d<FmtQ40>(dq, f, d, st, err);
+    case QT_Q4_K: return dispatch_fused_d<FmtQ4K>(dq, f, d, st, err);
+    case QT_Q5_K: return dispatch_fused_d<FmtQ5K>(dq, f, d, st, err);
+    case QT_Q6_K: return dispatch_fused_d<FmtQ6K>(dq, f, d, st, err);
+    default: return 0;
     }
 }
 
@@ -343,7 +469,7 @@ qmoe_status qmv(int qtype, const void* W, int64_t rows, int64_t cols, const floa
 size_t ffn_swiglu_workspace_size(int64_t hidden, int64_t inter) {
     (void)hidden;
     if (inter <= 0) return 0;
-    return static_cast<size_t>(align_up(static_cast<int>(inter * 4), 256));
+    return WS_SYNC_BYTES + static_cast<size_t>(align_up(static_cast<int>(inter * 4), 256));
 }
 
 static qmoe_status check_ffn_qtypes(const char* fn, int gq, int uq, int dq) {
@@ -386,7 +512,7 @@ qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int g
     DevInfo* d = nullptr;
     if (qmoe_status s = device_info(&d)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    float* a = static_cast<float*>(ws);
+    float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + WS_SYNC_BYTES);
 
     StreamParams pg = {};
     pg.units = inter;
@@ -398,7 +524,6 @@ qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int g
     pg.rb1 = row_bytes_of(up_qtype, hidden);
     pg.x = x;
     pg.out = a;
-    if (qmoe_status s = dispatch<MODE_GATEUP>(gate_qtype, pg, *d, st)) return s;
 
     StreamParams pd = {};
     pd.units = hidden;
@@ -408,6 +533,16 @@ qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int g
     pd.rb0 = row_bytes_of(down_qtype, inter);
     pd.x = a;
     pd.out = residual;
+
+    FusedParams f = {};
+    f.gu = pg;
+    f.dn = pd;
+    f.sync = static_cast<unsigned long long*>(ws);
+    qmoe_status ferr = QMOE_OK;
+    const int fr = dispatch_fused(gate_qtype, down_qtype, f, *d, st, &ferr);
+    if (fr < 0) return ferr;
+    if (fr > 0) return QMOE_OK;
+    if (qmoe_status s = dispatch<MODE_GATEUP>(gate_qtype, pg, *d, st)) return s;
     return dispatch<MODE_DOWN>(down_qtype, pd, *d, st);
 }
 
@@ -433,7 +568,7 @@ static PfWs pf_ws_layout(const qmoe_moe_shape* s) {
                  F = s->expert_dim;
     auto al = [](size_t v) { return (v + 255) / 256 * 256; };
     PfWs w;
-    size_t o = 0;
+    size_t o = WS_SYNC_BYTES;
     w.logits = o; o += al(T * E * 4);
     w.tidx = o;   o += al(T * K * 4);
     w.tw = o;     o += al(T * K * 4);
@@ -450,7 +585,7 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* s) {
     if (!s || s->n_tokens <= 0 || s->num_experts <= 0 || s->top_k <= 0 || s->expert_dim <= 0 ||
         s->hidden <= 0)
         return 0;
-    const size_t decode = moe_logits_bytes(s) +
+    const size_t decode = WS_SYNC_BYTES + moe_logits_bytes(s) +
                           static_cast<size_t>(align_up(s->top_k * s->expert_dim * 4, 256));
     if (prefill_path(s)) {
         const size_t pf = pf_ws_layout(s).total;
@@ -569,8 +704,9 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
                            topk_w, ws, *d, st);
 
     const int H = s.hidden, F = s.expert_dim, E = s.num_experts, K = s.top_k;
-    float* logits = static_cast<float*>(ws);
-    float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + moe_logits_bytes(&s));
+    float* logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + WS_SYNC_BYTES);
+    float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + WS_SYNC_BYTES +
+                                        moe_logits_bytes(&s));
     const int64_t grb = row_bytes_of(s.gate_qtype, H), urb = row_bytes_of(s.up_qtype, H);
     const int64_t drb = row_bytes_of(s.down_qtype, F);
 
@@ -578,7 +714,6 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
         const float* xt = x + static_cast<int64_t>(t) * H;
         float* rt = residual + static_cast<int64_t>(t) * H;
         float* lt = logits + static_cast<int64_t>(t) * E;
-        if (qmoe_status r = run_f32_gemv(router_W, xt, lt, E, H, st)) return r;
 
         StreamParams pg = {};
         pg.units = static_cast<int64_t>(K) * F;
@@ -599,7 +734,6 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
         pg.topk_idx_out = topk_idx ? topk_idx + static_cast<int64_t>(t) * K : nullptr;
         pg.topk_w_out = topk_w ? topk_w + static_cast<int64_t>(t) * K : nullptr;
         pg.moe = 1;
-        if (qmoe_status r = dispatch<MODE_GATEUP>(s.gate_qtype, pg, *d, st)) return r;
 
         StreamParams pd = {};
         pd.units = H;
@@ -615,6 +749,26 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
         pd.topk = K;
         pd.F = F;
         pd.moe = 1;
+
+        FusedParams f = {};
+        f.gu = pg;
+        f.dn = pd;
+        f.router = router_W;
+        f.logits = lt;
+        f.sync = static_cast<unsigned long long*>(ws);
+        f.moe = 1;
+        f.E = E;
+        f.H = H;
+        f.topk = K;
+        f.topk_idx_out = pg.topk_idx_out;
+        f.topk_w_out = pg.topk_w_out;
+        qmoe_status ferr = QMOE_OK;
+        const int fr = dispatch_fused(s.gate_qtype, s.down_qtype, f, *d, st, &ferr);
+        if (fr < 0) return ferr;
+        if (fr > 0) continue;
+        // the layer does not fit the fused kernel: router, gate/up, down
+        if (qmoe_status r = run_f32_gemv(router_W, xt, lt, E, H, st)) return r;
+        if (qmoe_status r = dispatch<MODE_GATEUP>(s.gate_qtype, pg, *d, st)) return r;
         if (qmoe_status r = dispatch<MODE_DOWN>(s.down_qtype, pd, *d, st)) return r;
     }
     return QMOE_OK;
@@ -679,6 +833,7 @@ qmoe_status qmoe_device_status(void* stream) {
         return fail(QMOE_ERR_TIMEOUT, "a bounded device wait expired (code %u: %s)", v,
                     v == DEV_TIMEOUT_FULL    ? "stage never filled"
                     : v == DEV_TIMEOUT_EMPTY ? "stage never released"
+                    : v == DEV_TIMEOUT_GRID  ? "grid barrier: not every CTA arrived"
                                              : "tensor-core pipeline stalled");
     }
     return QMOE_OK;

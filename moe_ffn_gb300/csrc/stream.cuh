@@ -17,6 +17,10 @@
 // kernel before it.  x, outputs and routing data are touched only after the
 // wait.
 //
+// The producer and consumer loops are device functions over a shared ring
+// (produce_phase / consume_phase), so one kernel can run several phases
+// back to back through the same stages (the fused FFN / MoE kernel).
+//
 // Modes:
 //   QMV     y[r] = W[r] . x                         (overwrite)           R = 4
 //   GATEUP  a[j] = w_s * silu(G_e[jj].x) * (U_e[jj].x),  j = s*F + jj      R = 4
@@ -105,20 +109,39 @@ __host__ __device__ inline SmemLayout smem_layout(const StreamParams& p) {
 // "aprender-serve 0.70.2 — forward_qwen3_moe_resident.rs" (module doc,
 // moe_layer).  The renormalised weight of a selected expert equals
 // exp(l_s - l_max) / sum over the selected k of exp(l_t - l_max).
-// All threads of the CTA must call it.
-__device__ inline void route_topk_cta(const float* __restrict__ logits, int E, int k,
-                                      float* s_logit, int32_t* s_idx, float* s_w) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    for (int e = tid; e < E; e += nt) s_logit[e] = __ldcg(logits + e);
-    __syncthreads();
+// Threads [0, nthr) of the CTA call it together; they synchronise on named
+// barrier `bar` (0: the whole CTA, nthr == blockDim.x).  k <= 32.
+__device__ __forceinline__ void group_sync(int bar, int nthr) {
+    if (bar == 0)
+        __syncthreads();
+    else
+        named_bar(bar, nthr);
+}
+
+__device__ inline void route_topk(const float* __restrict__ logits, int E, int k, float* s_logit,
+                                  int32_t* s_idx, float* s_w, int tid, int nthr, int bar) {
+    for (int e = tid; e < E; e += nthr) s_logit[e] = __ldcg(logits + e);
+    group_sync(bar, nthr);
     // two threads per expert: each counts the experts that beat it over half of E
-    for (int base = 0; base < E; base += nt / 2) {
+    for (int base = 0; base < E; base += nthr / 2) {
         const int e = base + tid / 2, half = tid & 1;
         int rank = 0;
         if (e < E) {
             const float v = s_logit[e];
             const int u0 = half ? E / 2 : 0, u1 = half ? E : E / 2;
-            for (int u = u0; u < u1; ++u) {
+            int u = u0;
+            if ((E & 7) == 0) {  // both halves are whole float4s
+                const float4* l4 = reinterpret_cast<const float4*>(s_logit);
+#pragma unroll 4
+                for (; u < u1; u += 4) {
+                    const float4 w = l4[u >> 2];
+                    rank += (w.x > v) || (w.x == v && u < e);
+                    rank += (w.y > v) || (w.y == v && u + 1 < e);
+                    rank += (w.z > v) || (w.z == v && u + 2 < e);
+                    rank += (w.w > v) || (w.w == v && u + 3 < e);
+                }
+            }
+            for (; u < u1; ++u) {
                 const float w = s_logit[u];
                 rank += (w > v) || (w == v && u < e);
             }
@@ -126,86 +149,75 @@ __device__ inline void route_topk_cta(const float* __restrict__ logits, int E, i
         rank += __shfl_xor_sync(0xffffffffu, rank, 1);
         if (e < E && half == 0 && rank < k) s_idx[rank] = e;
     }
-    __syncthreads();
-    if (tid == 0) {
-        const float lmax = s_logit[s_idx[0]];
-        float z = 0.f;
-        for (int s = 0; s < k; ++s) {
-            const float p = expf(s_logit[s_idx[s]] - lmax);
-            s_w[s] = p;
-            z += p;
-        }
-        const float inv = 1.0f / z;
-        for (int s = 0; s < k; ++s) s_w[s] *= inv;
+    group_sync(bar, nthr);
+    if (tid < 32) {
+        const float l = tid < k ? s_logit[s_idx[tid]] : 0.f;
+        const float lmax = __shfl_sync(0xffffffffu, l, 0);
+        const float pr = tid < k ? expf(l - lmax) : 0.f;
+        float z = pr;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (tid < k) s_w[tid] = pr / z;
     }
-    __syncthreads();
+    group_sync(bar, nthr);
 }
 
 template <class Fmt>
 __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, float* xq,
                                     float* xs, int tid, int nthreads) {
     // x' in the per-quarter interleaved order; xs = sum of x per 16 elements.
-    // Every x' float4 slot (group g, i4, quarter q) holds four consecutive,
-    // 16-byte-aligned elements of x (the formats' element orders keep
-    // i = 4*i4 .. 4*i4+3 contiguous), each scaled by its own power of two.
-    // Loads are batched (UNR in flight per thread) before any use.
-    constexpr int UNR = 8;
-    const int n4 = ngroups * 64;
+    // A thread takes 16-element chunks of x: it loads the chunk's four
+    // aligned float4s (all loads in flight before any use, so the table
+    // costs one L2 round trip), stores their sum to xs, and scatters each
+    // float4 to its x' slot (the formats' element orders keep every slot
+    // four consecutive elements), each element scaled by its own power of two.
+    constexpr int UNR = 4;
+    const int n16 = ngroups * 16;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     float4* xq4 = reinterpret_cast<float4*>(xq);
-    for (int base = tid; base < n4; base += nthreads * UNR) {
-        float4 v[UNR];
+    for (int base = tid; base < n16; base += nthreads * UNR) {
+        float4 v[UNR][4];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
-            const int f = base + u * nthreads;
-            if (f < n4) {
-                const int g = f >> 6, i4 = (f >> 2) & 15, q = f & 3;
-                v[u] = __ldcg(x4 + ((g * 256 + Fmt::elem(q, 4 * i4)) >> 2));
+            const int c = base + u * nthreads;
+            if (c < n16) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[u][k] = __ldcg(x4 + 4 * c + k);
             }
         }
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
-            const int f = base + u * nthreads;
-            if (f < n4) {
-                const int i4 = (f >> 2) & 15, q = f & 3, i = 4 * i4;
-                float4 o;
-                o.x = v[u].x * xprime_scale(Fmt::pos(q, i));
-                o.y = v[u].y * xprime_scale(Fmt::pos(q, i + 1));
-                o.z = v[u].z * xprime_scale(Fmt::pos(q, i + 2));
-                o.w = v[u].w * xprime_scale(Fmt::pos(q, i + 3));
-                xq4[f] = o;
-            }
-        }
-    }
-    const int n16 = ngroups * 16;
-    for (int base = tid; base < n16; base += nthreads * 2) {
-        float4 v[2][4];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int g16 = base + u * nthreads;
-            if (g16 < n16) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) v[u][k] = __ldcg(x4 + g16 * 4 + k);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int g16 = base + u * nthreads;
-            if (g16 < n16) {
+            const int c = base + u * nthreads;
+            if (c < n16) {
                 float s = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) s += (v[u][k].x + v[u][k].y) + (v[u][k].z + v[u][k].w);
-                xs[g16] = s;
+                xs[c] = s;
+                const int g = c >> 4;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int slot = Fmt::xslot(4 * (c & 15) + k);
+                    const int q = slot & 3, i = 4 * (slot >> 2);
+                    float4 o;
+                    o.x = v[u][k].x * xprime_scale(Fmt::pos(q, i));
+                    o.y = v[u][k].y * xprime_scale(Fmt::pos(q, i + 1));
+                    o.z = v[u][k].z * xprime_scale(Fmt::pos(q, i + 2));
+                    o.w = v[u][k].w * xprime_scale(Fmt::pos(q, i + 3));
+                    xq4[g * 64 + slot] = o;
+                }
             }
         }
     }
 }
 
 // Address of the bytes of (row slot r, k-segment ks) for the tile starting
-// at unit u0; nullptr if the row's unit is outside [.., uend).
+// at unit u0; nullptr if the row's unit is outside [.., uend).  For the MoE
+// gate/up product s0 = u0 / F, the routed slot of the tile's first unit
+// (a tile spans fewer than F units, so it crosses at most one slot border).
 template <int MODE>
 __device__ __forceinline__ const uint8_t* row_addr(const StreamParams& p, const int32_t* s_idx,
-                                                   int64_t u0, int64_t uend, int r, int ks) {
+                                                   int64_t u0, int s0, int64_t uend, int r,
+                                                   int ks) {
     const int g = r & 7, rr = r >> 3;
     if (MODE == MODE_GATEUP) {
         const bool up = rr >= 2;
@@ -214,8 +226,12 @@ __device__ __forceinline__ const uint8_t* row_addr(const StreamParams& p, const 
         const uint8_t* base = up ? p.W1 : p.W0;
         const int64_t rb = up ? p.rb1 : p.rb0, es = up ? p.es1 : p.es0;
         if (p.moe) {
-            const int s = static_cast<int>(u / p.F);
-            const int64_t jj = u - static_cast<int64_t>(s) * p.F;
+            int64_t jj = u - static_cast<int64_t>(s0) * p.F;
+            int s = s0;
+            if (jj >= p.F) {
+                jj -= p.F;
+                ++s;
+            }
             return base + static_cast<int64_t>(s_idx[s]) * es + jj * rb;
         }
         return base + u * rb;
@@ -248,117 +264,105 @@ __device__ __forceinline__ ChunkDesc chunk_desc(const StreamParams& p, int c) {
     return d;
 }
 
+// The stage ring: nstages stages of stage_bytes, a full barrier (one
+// arrival + transaction bytes) and an empty barrier (NCW consumer warps)
+// per stage.  Producer and consumers number chunks with one running count
+// `it` across phases, so phases of different geometry can follow each other
+// through the same ring.
+struct Ring {
+    uint8_t* stages;
+    uint64_t* full;
+    uint64_t* empty;
+    int nstages, stage_bytes;
+};
+
+template <int MODE>
+__device__ __forceinline__ int tile_slot(const StreamParams& p, int64_t u0) {
+    return (MODE == MODE_GATEUP && p.moe) ? static_cast<int>(static_cast<uint32_t>(u0) /
+                                                             static_cast<uint32_t>(p.F))
+                                          : 0;
+}
+
+// Producer warp: stream every chunk of the units [ubeg, uend) into the ring.
+// False if a wait for a free stage timed out (the error word is set).
 template <class Fmt, int MODE>
-__global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamParams p) {
+__device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int32_t* s_idx,
+                              int64_t ubeg, int64_t uend, int& it, int lane) {
     using G = ModeGeom<MODE>;
-    constexpr int R = G::R;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const SmemLayout L = smem_layout(p);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
-    int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.off_tidx);
-    float* s_w = reinterpret_cast<float*>(smem + L.off_tw);
-    float* s_logit = reinterpret_cast<float*>(smem + L.off_logit);
-    float* part = reinterpret_cast<float*>(smem + L.off_part);
-    float* xs = reinterpret_cast<float*>(smem + L.off_xs);
-    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
-    uint8_t* stages = smem + L.off_stage;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t cta = blockIdx.x, ncta = gridDim.x;
-    const int64_t ubeg = p.units * cta / ncta, uend = p.units * (cta + 1) / ncta;
-
-    if (tid == 0) {
-        for (int s = 0; s < p.nstages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NCW);
-        }
-        fence_barrier_init();
-    }
-    // Routing decides which expert rows are streamed.  The down product's
-    // logits come from the router kernel two launches back, complete before
-    // this grid was allowed to start; the gate/up kernel reads them right
-    // after its own dependency wait.
-    if (p.moe && MODE == MODE_DOWN) {
-        route_topk_cta(p.logits, p.E, p.topk, s_logit, s_idx, s_w);
-    } else if (p.moe && MODE == MODE_GATEUP) {
-        pdl_wait();
-        pdl_trigger();
-        route_topk_cta(p.logits, p.E, p.topk, s_logit, s_idx, s_w);
-        if (blockIdx.x == 0 && tid < p.topk) {
-            if (p.topk_idx_out) p.topk_idx_out[tid] = s_idx[tid];
-            if (p.topk_w_out) p.topk_w_out[tid] = s_w[tid];
-        }
-    } else {
-        __syncthreads();
-    }
-
+    const uint64_t pol = policy_evict_first();
     const int ntiles = static_cast<int>((uend - ubeg + G::TU - 1) / G::TU);
-
-    if (warp == NCW) {
-        // ------------------------------------------------------ producer
-        const uint64_t pol = policy_evict_first();
-        int it = 0;
-        for (int t = 0; t < ntiles; ++t) {
-            const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
-            for (int c = 0; c < p.n_chunk; ++c, ++it) {
-                const int s = it % p.nstages;
-                const int round = it / p.nstages;
-                if (round > 0 &&
-                    !mbar_wait_bounded(&empty[s], (round - 1) & 1, p.err, DEV_TIMEOUT_EMPTY))
-                    return;
-                const ChunkDesc cd = chunk_desc(p, c);
-                const int ncopy = G::ROWS * cd.nks;
-                const uint32_t seg_bytes = static_cast<uint32_t>(cd.nbp * Fmt::SBB);
-                uint32_t mine = 0;
-                for (int k = lane; k < ncopy; k += 32) {
-                    const int r = k / cd.nks, pk = k % cd.nks;
-                    const uint8_t* a = row_addr<MODE>(p, s_idx, u0, uend, r, cd.ks0 + pk);
-                    if (a) {
-                        const uintptr_t src = reinterpret_cast<uintptr_t>(a) +
-                                              static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
-                        const uintptr_t lo = src & ~uintptr_t(15);
-                        mine += static_cast<uint32_t>(((src + seg_bytes + 15) & ~uintptr_t(15)) - lo);
-                    }
+    for (int t = 0; t < ntiles; ++t) {
+        const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
+        const int s0 = tile_slot<MODE>(p, u0);
+        for (int c = 0; c < p.n_chunk; ++c, ++it) {
+            const int s = it % ring.nstages;
+            const int round = it / ring.nstages;
+            if (round > 0 &&
+                !mbar_wait_bounded(&ring.empty[s], (round - 1) & 1, p.err, DEV_TIMEOUT_EMPTY))
+                return false;
+            const ChunkDesc cd = chunk_desc(p, c);
+            const int ncopy = G::ROWS * cd.nks;
+            const uint32_t seg_bytes = static_cast<uint32_t>(cd.nbp * Fmt::SBB);
+            uint32_t mine = 0;
+            for (int k = lane; k < ncopy; k += 32) {
+                const int r = k / cd.nks, pk = k % cd.nks;
+                const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, r, cd.ks0 + pk);
+                if (a) {
+                    const uintptr_t src = reinterpret_cast<uintptr_t>(a) +
+                                          static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
+                    const uintptr_t lo = src & ~uintptr_t(15);
+                    mine += static_cast<uint32_t>(((src + seg_bytes + 15) & ~uintptr_t(15)) - lo);
                 }
+            }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], mine);
-                __syncwarp();
-                uint8_t* st = stages + static_cast<size_t>(s) * p.stage_bytes;
-                for (int k = lane; k < ncopy; k += 32) {
-                    const int r = k / cd.nks, pk = k % cd.nks;
-                    const uint8_t* a = row_addr<MODE>(p, s_idx, u0, uend, r, cd.ks0 + pk);
-                    if (a) {
-                        const uintptr_t src = reinterpret_cast<uintptr_t>(a) +
-                                              static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
-                        const uintptr_t lo = src & ~uintptr_t(15);
-                        const uint32_t n =
-                            static_cast<uint32_t>(((src + seg_bytes + 15) & ~uintptr_t(15)) - lo);
-                        bulk_g2s(st + r * p.slot_stride + pk * p.piece_stride,
-                                 reinterpret_cast<const void*>(lo), n, &full[s], pol);
-                    }
+            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            if (lane == 0) mbar_arrive_expect_tx(&ring.full[s], mine);
+            __syncwarp();
+            uint8_t* st = ring.stages + static_cast<size_t>(s) * ring.stage_bytes;
+            for (int k = lane; k < ncopy; k += 32) {
+                const int r = k / cd.nks, pk = k % cd.nks;
+                const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, r, cd.ks0 + pk);
+                if (a) {
+                    const uintptr_t src = reinterpret_cast<uintptr_t>(a) +
+                                          static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
+                    const uintptr_t lo = src & ~uintptr_t(15);
+                    const uint32_t n =
+                        static_cast<uint32_t>(((src + seg_bytes + 15) & ~uintptr_t(15)) - lo);
+                    bulk_g2s(st + r * p.slot_stride + pk * p.piece_stride,
+                             reinterpret_cast<const void*>(lo), n, &ring.full[s], pol);
                 }
             }
         }
-        return;
     }
-
-    // ---------------------------------------------------------- consumers
-    if (!(p.moe && MODE == MODE_GATEUP)) {  // the MoE gate/up grid waited above
-        pdl_wait();
-        pdl_trigger();
-    }
-    build_xprime<Fmt>(p.x, p.nb_seg * p.n_kseg, xq, xs, tid, NCW * 32);
-    named_bar(1, NCW * 32);
-
-    const int v = warp;
+    return true;
+}
+// Consumer warps 0..NCW-1: reduce every tile of [ubeg, uend) and write the
+// outputs (QMV: y = W.x; GATEUP: a = w * silu(g) * u; DOWN: out += D.a).
+// x' / xs must already hold the phase's input.  False (in every consumer
+// thread alike) if a stage wait timed out: a warp whose wait expired skips
+// the rest of its waits and arithmetic but still takes part in every named
+// barrier, so no warp is left waiting, and no output of a tile is written
+// unless every warp's data for it arrived.
+template <class Fmt, int MODE>
+__device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int32_t* s_idx,
+                              const float* s_w, const float* xq, const float* xs, float* part,
+                              int64_t ubeg, int64_t uend, int& it, int tid) {
+    using G = ModeGeom<MODE>;
+    constexpr int R = G::R;
+    const int v = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
     const float4* xq4 = reinterpret_cast<const float4*>(xq);
-    int it = 0;
+    const int ntiles = static_cast<int>((uend - ubeg + G::TU - 1) / G::TU);
     bool ok = true;
-    for (int t = 0; t < ntiles && ok; ++t) {
+    // Gate/up tiles with K <= 8 groups give a warp the same group in every
+    // tile: its x' stays in registers.  Elsewhere groups change each call,
+    // and keeping x' live would only cost registers.
+    constexpr bool KEEP_X = MODE == MODE_GATEUP;
+    float x[64];
+    int xg = -1;
+    for (int t = 0; t < ntiles; ++t) {
         const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
+        const int s0 = tile_slot<MODE>(p, u0);
         float acc[R];
         // low 32 bits of each row's address (k-segment 0): only the 16-byte
         // phase is needed to find the row inside its staged slot
@@ -366,28 +370,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             acc[rr] = 0.f;
-            const uint8_t* a = row_addr<MODE>(p, s_idx, u0, uend, rr * 8 + g, 0);
+            const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, rr * 8 + g, 0);
             rowlo[rr] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a));
             if (MODE == MODE_DOWN && p.moe && a)  // k-segment 0's expert offset removed
                 rowlo[rr] -= static_cast<uint32_t>(s_idx[0]) * static_cast<uint32_t>(p.es0);
         }
         for (int c = 0; c < p.n_chunk; ++c, ++it) {
-            const int s = it % p.nstages;
-            const int round = it / p.nstages;
-            if (!mbar_wait_bounded(&full[s], round & 1, p.err, DEV_TIMEOUT_FULL)) {
+            const int s = it % ring.nstages;
+            const int round = it / ring.nstages;
+            if (ok && !mbar_wait_bounded(&ring.full[s], round & 1, p.err, DEV_TIMEOUT_FULL))
                 ok = false;
-                break;
-            }
+            ok = __all_sync(0xffffffffu, ok);  // one decision per warp
             const ChunkDesc cd = chunk_desc(p, c);
-            const uint8_t* st = stages + static_cast<size_t>(s) * p.stage_bytes;
-            const int ntot = cd.nks * cd.nbp;
+            const uint8_t* st = ring.stages + static_cast<size_t>(s) * ring.stage_bytes;
+            const int ntot = ok ? cd.nks * cd.nbp : 0;
             const uint32_t b0off = static_cast<uint32_t>(cd.b0) * Fmt::SBB;
             for (int tt = v; tt < ntot; tt += G::WK) {
                 const int pk = tt / cd.nbp, bb = tt - pk * cd.nbp;
                 const int ks = cd.ks0 + pk, b = cd.b0 + bb;
                 const int gidx = ks * p.nb_seg + b;
-                float x[64];
-                load_xq(xq4 + gidx * 64, q, x);
+                if (!KEEP_X || gidx != xg) {
+                    load_xq(xq4 + gidx * 64, q, x);
+                    xg = gidx;
+                }
                 const float* xsg = xs + gidx * 16;
                 const uint32_t ksoff =
                     (MODE == MODE_DOWN && p.moe)
@@ -405,9 +410,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
                 Fmt::template dotR<R>(sbp, q, x, xsg, acc);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&ring.empty[s]);
         }
-        if (!ok) break;
         float* pt = part + (t & 1) * NCW * MAX_ROWS;
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
@@ -416,28 +420,110 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             if (q == 0) pt[v * MAX_ROWS + rr * 8 + g] = a;
         }
-        named_bar(1, NCW * 32);
-        const int ct = tid;
-        if (ct < G::TU && u0 + ct < uend) {
-            const int64_t u = u0 + ct;
-            if (MODE == MODE_GATEUP) {
-                float gs = 0.f, us = 0.f;
-                for (int k = 0; k < G::WK; ++k) {
-                    gs += pt[k * MAX_ROWS + ct];
-                    us += pt[k * MAX_ROWS + G::TU + ct];
+        ok = named_bar_and(1, NCW * 32, ok);
+        // cross-warp sums as shuffle trees: eight consecutive lanes hold the
+        // eight warps' partials of one row
+        const int k8 = tid & 7;
+        if (MODE == MODE_GATEUP) {
+            // lanes 0-7 of a 16-lane group: gate row of unit uu; 8-15: its up row
+            const int uu = tid >> 4, up = (tid >> 3) & 1;
+            float vs = pt[k8 * MAX_ROWS + up * G::TU + uu];
+            vs += __shfl_xor_sync(0xffffffffu, vs, 1);
+            vs += __shfl_xor_sync(0xffffffffu, vs, 2);
+            vs += __shfl_xor_sync(0xffffffffu, vs, 4);
+            const float us = __shfl_down_sync(0xffffffffu, vs, 8);
+            const int64_t u = u0 + uu;
+            if (ok && up == 0 && k8 == 0 && u < uend) {
+                float w = 1.0f;
+                if (p.moe) {
+                    const int sl = s0 + (u - static_cast<int64_t>(s0) * p.F >= p.F ? 1 : 0);
+                    w = s_w[sl];
                 }
-                const float w = p.moe ? s_w[static_cast<int>(u / p.F)] : 1.0f;
-                p.out[u] = w * ((gs / (1.0f + expf(-gs))) * us);
-            } else {
-                float y = 0.f;
-                for (int k = 0; k < G::WK; ++k) y += pt[k * MAX_ROWS + ct];
+                p.out[u] = w * ((vs / (1.0f + expf(-vs))) * us);
+            }
+        } else {
+            const int r = tid >> 3;
+            float vs = r < G::ROWS ? pt[k8 * MAX_ROWS + r] : 0.f;
+            vs += __shfl_xor_sync(0xffffffffu, vs, 1);
+            vs += __shfl_xor_sync(0xffffffffu, vs, 2);
+            vs += __shfl_xor_sync(0xffffffffu, vs, 4);
+            const int64_t u = u0 + r;
+            if (ok && k8 == 0 && r < G::TU && u < uend) {
                 if (MODE == MODE_QMV)
-                    p.out[u] = y;
+                    p.out[u] = vs;
                 else
-                    p.out[u] += y;
+                    p.out[u] += vs;
             }
         }
     }
+    return ok;
+}
+
+template <class Fmt, int MODE>
+__global__ void __launch_bounds__(NTHREADS) stream_gemv_kernel(const StreamParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const SmemLayout L = smem_layout(p);
+    Ring ring;
+    ring.full = reinterpret_cast<uint64_t*>(smem + L.off_full);
+    ring.empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
+    ring.stages = smem + L.off_stage;
+    ring.nstages = p.nstages;
+    ring.stage_bytes = p.stage_bytes;
+    int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.off_tidx);
+    float* s_w = reinterpret_cast<float*>(smem + L.off_tw);
+    float* s_logit = reinterpret_cast<float*>(smem + L.off_logit);
+    float* part = reinterpret_cast<float*>(smem + L.off_part);
+    float* xs = reinterpret_cast<float*>(smem + L.off_xs);
+    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t cta = blockIdx.x, ncta = gridDim.x;
+    const int64_t ubeg = p.units * cta / ncta, uend = p.units * (cta + 1) / ncta;
+
+    // The producer's lane 0 initialises the stage barriers.  Without routing
+    // the producer starts streaming at once and only arrives on named
+    // barrier 2; the consumers sync on it before their first stage wait.
+    // With routing every thread takes part in route_topk, whose
+    // __syncthreads also publishes the barriers.
+    if (tid == NCW * 32) {
+        for (int s = 0; s < p.nstages; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], NCW);
+        }
+        fence_barrier_init();
+    }
+    // Routing decides which expert rows are streamed.  The down product's
+    // logits come from the router kernel two launches back, complete before
+    // this grid was allowed to start; the gate/up kernel reads them right
+    // after its own dependency wait.
+    if (p.moe && MODE == MODE_DOWN) {
+        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0);
+    } else if (p.moe && MODE == MODE_GATEUP) {
+        pdl_wait();
+        pdl_trigger();
+        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0);
+        if (blockIdx.x == 0 && tid < p.topk) {
+            if (p.topk_idx_out) p.topk_idx_out[tid] = s_idx[tid];
+            if (p.topk_w_out) p.topk_w_out[tid] = s_w[tid];
+        }
+    } else if (warp == NCW) {
+        __syncwarp();
+        named_bar_arrive(2, NTHREADS);
+    }
+
+    int it = 0;
+    if (warp == NCW) {
+        produce_phase<Fmt, MODE>(p, ring, s_idx, ubeg, uend, it, lane);
+        return;
+    }
+    if (!(p.moe && MODE == MODE_GATEUP)) {  // the MoE gate/up grid waited above
+        pdl_wait();
+        pdl_trigger();
+    }
+    build_xprime<Fmt>(p.x, p.nb_seg * p.n_kseg, xq, xs, tid, NCW * 32);
+    named_bar(1, NCW * 32);
+    if (!p.moe) named_bar(2, NTHREADS);  // the stage barriers are initialised
+    consume_phase<Fmt, MODE>(p, ring, s_idx, s_w, xq, xs, part, ubeg, uend, it, tid);
 }
 
 }  // namespace qmoe
