@@ -56,6 +56,12 @@ def barrier(world):
         dist.barrier()
 
 
+def job_throughput(bytes_per_rank_step, ms_per_step, world):
+    """Whole-job GB/s: every rank moved bytes_per_rank_step per step, and a
+    step took ms_per_step (the slowest rank's time)."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def max_over_ranks(v, world, device=None):
     """Max of a float across ranks (all-reduce MAX); identity for one rank."""
     if world == 1:
@@ -167,7 +173,7 @@ def run_ours(args, rank, world):
     barrier(world)
     ms_total = max_over_ranks(ms_local, world, dev)
     ms_step = ms_total / steps_timed
-    value = world * alg_step / (ms_step * 1e-3) / 1e9
+    value = job_throughput(alg_step, ms_step, world)
 
     # ---- per-format kernel timing (dominant kernel roofline): L launches
     # back to back in a graph on the launching stream, rotating copies
@@ -219,7 +225,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
-    e2e_value = world * alg_step / (e2e_ms * 1e-3) / 1e9
+    e2e_value = job_throughput(alg_step, e2e_ms, world)
 
     del copies, g_sweep
     torch.cuda.empty_cache()
@@ -311,6 +317,12 @@ def load_traffic(key):
     return None
 
 
+def layer_launches(separate):
+    """Kernel launches per FFN layer / MoE token: one fused cooperative launch,
+    or `separate` when QMOE_FUSED=0 selects the separate-kernel form."""
+    return separate if os.environ.get("QMOE_FUSED", "1").startswith("0") else 1
+
+
 def bench_layers(qm, synth, dev, stream, args):
     """MoE decode (us/token), dense FFN (us/call), MoE 512-token layer
     (us/token); each captured in a CUDA graph and replayed."""
@@ -345,7 +357,8 @@ def bench_layers(qm, synth, dev, stream, args):
            + 3 * shp["hidden"] * 4)
     out["moe_decode"] = {"us_per_token": round(us, 3), "alg_bytes": alg,
                          "gbs": round(alg / us / 1e3, 1), "frac": round(alg / us / 1e3 / peak, 3),
-                         "launches_per_token": 3, "launch": f"CUDA graph of {n} tokens",
+                         "launches_per_token": layer_launches(3),
+                         "launch": f"CUDA graph of {n} tokens",
                          "workload": "hidden 2048, 128 experts, top-8, expert_dim 768, Q4_K/Q4_K/Q6_K"}
     del d, inp, gm
     torch.cuda.empty_cache()
@@ -372,7 +385,7 @@ def bench_layers(qm, synth, dev, stream, args):
     us = time_replays(torch, gf, 4) * 1e3 / (4 * n)
     alg = fin["gate"].nbytes + fin["up"].nbytes + fin["down"].nbytes + 4 * w["hidden"] * 3
     out["dense_ffn"] = {"us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1),
-                        "frac": round(alg / us / 1e3 / peak, 3), "launches": 2,
+                        "frac": round(alg / us / 1e3 / peak, 3), "launches": layer_launches(2),
                         "launch": f"CUDA graph of {n} calls",
                         "workload": "hidden 4096, intermediate 14336, Q4_K/Q4_K/Q6_K"}
     del G, U, D, gf

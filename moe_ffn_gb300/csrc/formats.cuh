@@ -117,6 +117,10 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
 // nibbles come from the multiply pipe (top_field, __umulhi): both at bit 0.
 struct FmtQ4K {
     static constexpr int SBB = 144;
+    // Rows may sit at their global stride in shared memory (runs): the
+    // lanes' 128-bit loads of two rows conflict at most two ways.  Formats
+    // read with 32-bit loads would conflict eight ways.
+    static constexpr bool RUNS_OK = true;
     // Row slot stride wanted modulo 128 bytes (-1: any odd multiple of 16)
     static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) {
@@ -138,8 +142,8 @@ struct FmtQ4K {
     // ferrox_q4_k_scale_min, four pairs per 32-bit word: pairs 0..3 are the
     // low 6 bits of bytes 0..3 (sc) and 4..7 (m); pairs 4..7 join the low /
     // high nibble of bytes 8..11 with the top two bits of bytes 0..3 / 4..7.
-    // The lane's word is selected branch-free; bytes become floats on the
-    // conversion pipe.
+    // The lane's word is selected branch-free; a byte becomes a float by a
+    // byte permute into the mantissa of 2^23 and one subtraction.
     __device__ __forceinline__ static void scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int q,
                                                      float& sca, float& ma, float& scb,
                                                      float& mb) {
@@ -148,11 +152,11 @@ struct FmtQ4K {
             ((hi ? s2 : s0) & 0x0F0F0F0Fu) | ((hi ? (s0 >> 2) : s0) & 0x30303030u);
         const uint32_t m_w =
             ((hi ? (s2 >> 4) : s1) & 0x0F0F0F0Fu) | ((hi ? (s1 >> 2) : s1) & 0x30303030u);
-        const int sh = 16 * (q & 1);  // pairs 2q, 2q+1 are bytes 2(q&1), 2(q&1)+1
-        sca = static_cast<float>((sc_w >> sh) & 0xFFu);
-        scb = static_cast<float>((sc_w >> (sh + 8)) & 0xFFu);
-        ma = static_cast<float>((m_w >> sh) & 0xFFu);
-        mb = static_cast<float>((m_w >> (sh + 8)) & 0xFFu);
+        const uint32_t ia = 0x7540u | (2u * (q & 1)), ib = ia + 1u;
+        sca = __int_as_float(__byte_perm(sc_w, 0x4B000000u, ia)) - 8388608.f;
+        scb = __int_as_float(__byte_perm(sc_w, 0x4B000000u, ib)) - 8388608.f;
+        ma = __int_as_float(__byte_perm(m_w, 0x4B000000u, ia)) - 8388608.f;
+        mb = __int_as_float(__byte_perm(m_w, 0x4B000000u, ib)) - 8388608.f;
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
@@ -200,11 +204,13 @@ struct FmtQ4K {
 // 176-byte super-block: d @0, dmin @2, scales @4, qh[32] @16, qs[128] @48.
 // As Q4_K, plus 16 where bit 2q (low half) / 2q+1 (high half) of qh[l] is
 // set.  The qh bit is rotated into bit 4 of each byte and merged with the
-// nibble (bits 5..7 of the merge are don't-care: the 5-bit mask drops them).
+// nibble; bits 5..7 of every merged byte are zero, so byte 3's field is
+// one shift.
 // Lane element order as Q4_K; positions: byte k -> 8k for k<3, byte 3's
-// field from the multiply pipe -> 0.
+// field shifted down -> 0.
 struct FmtQ5K {
     static constexpr int SBB = 176;
+    static constexpr bool RUNS_OK = true;
     static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) { return FmtQ4K::elem(q, i); }
     __host__ __device__ static int xslot(int e4) { return FmtQ4K::xslot(e4); }
@@ -241,13 +247,13 @@ struct FmtQ5K {
             for (int r = 0; r < R; ++r) {
                 const uint32_t w = W[r][t], hw = H[r][t];
                 const uint32_t lo =
-                    (w & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rlo) & 0xF0F0F0F0u);
+                    (w & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rlo) & 0x10101010u);
                 const uint32_t hi =
-                    ((w >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rhi) & 0xF0F0F0F0u);
+                    ((w >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rhi) & 0x10101010u);
                 alo[r] = qfma2(lo & 0x1Fu, lo & 0x1F00u, x[8 * t], x[8 * t + 1], alo[r]);
-                alo[r] = qfma2(lo & 0x1F0000u, top_field<5>(lo), x[8 * t + 2], x[8 * t + 3], alo[r]);
+                alo[r] = qfma2(lo & 0x1F0000u, lo >> 24, x[8 * t + 2], x[8 * t + 3], alo[r]);
                 ahi[r] = qfma2(hi & 0x1Fu, hi & 0x1F00u, x[8 * t + 4], x[8 * t + 5], ahi[r]);
-                ahi[r] = qfma2(hi & 0x1F0000u, top_field<5>(hi), x[8 * t + 6], x[8 * t + 7], ahi[r]);
+                ahi[r] = qfma2(hi & 0x1F0000u, hi >> 24, x[8 * t + 6], x[8 * t + 7], ahi[r]);
             }
         }
         const float Xa = xs16[4 * q] + xs16[4 * q + 1];
@@ -272,9 +278,11 @@ struct FmtQ5K {
 // sc[8h + c + {0,2,4,6}]; value (d*sc)*(q-32).  Super-blocks are only
 // 2-byte aligned, so words are read with funnel shifts.
 // Lane element order: i = 16u + 4t + j -> element 128h + 32t + 16c + 4u + j;
-// positions (0, 8, 16, 0) (byte 3's field from the multiply pipe).
+// positions (0, 8, 16, 0).  The 6-bit values are merged with bits 6..7 of
+// every byte zero, so byte 3's field is one shift.
 struct FmtQ6K {
     static constexpr int SBB = 210;
+    static constexpr bool RUNS_OK = true;
     // 32 mod 128: the aligned loads of two row groups in a quarter-warp
     // fall in disjoint 16-byte bank groups
     static constexpr int SLOT_REM128 = 32;
@@ -377,19 +385,19 @@ struct FmtQ6K {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t av = A[r][u], bv = B[r][u], hv = H[r][u];
-                const uint32_t v0 = (av & 0x0F0F0F0Fu) | ((hv << 4) & 0xF0F0F0F0u);
-                const uint32_t v1 = (bv & 0x0F0F0F0Fu) | ((hv << 2) & 0xF0F0F0F0u);
-                const uint32_t v2 = ((av >> 4) & 0x0F0F0F0Fu) | (hv & 0xF0F0F0F0u);
-                const uint32_t v3 = ((bv >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0xF0F0F0F0u);
+                const uint32_t v0 = (av & 0x0F0F0F0Fu) | ((hv << 4) & 0x30303030u);
+                const uint32_t v1 = (bv & 0x0F0F0F0Fu) | ((hv << 2) & 0x30303030u);
+                const uint32_t v2 = ((av >> 4) & 0x0F0F0F0Fu) | (hv & 0x30303030u);
+                const uint32_t v3 = ((bv >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0x30303030u);
                 const float* xu = x + 16 * u;
                 a0[r] = qfma2(v0 & 0x3Fu, v0 & 0x3F00u, xu[0], xu[1], a0[r]);
-                a0[r] = qfma2(v0 & 0x3F0000u, top_field<6>(v0), xu[2], xu[3], a0[r]);
+                a0[r] = qfma2(v0 & 0x3F0000u, v0 >> 24, xu[2], xu[3], a0[r]);
                 a1[r] = qfma2(v1 & 0x3Fu, v1 & 0x3F00u, xu[4], xu[5], a1[r]);
-                a1[r] = qfma2(v1 & 0x3F0000u, top_field<6>(v1), xu[6], xu[7], a1[r]);
+                a1[r] = qfma2(v1 & 0x3F0000u, v1 >> 24, xu[6], xu[7], a1[r]);
                 a2[r] = qfma2(v2 & 0x3Fu, v2 & 0x3F00u, xu[8], xu[9], a2[r]);
-                a2[r] = qfma2(v2 & 0x3F0000u, top_field<6>(v2), xu[10], xu[11], a2[r]);
+                a2[r] = qfma2(v2 & 0x3F0000u, v2 >> 24, xu[10], xu[11], a2[r]);
                 a3[r] = qfma2(v3 & 0x3Fu, v3 & 0x3F00u, xu[12], xu[13], a3[r]);
-                a3[r] = qfma2(v3 & 0x3F0000u, top_field<6>(v3), xu[14], xu[15], a3[r]);
+                a3[r] = qfma2(v3 & 0x3F0000u, v3 >> 24, xu[14], xu[15], a3[r]);
             }
         }
         // 16-element groups of this lane: 8h + 2t + c
@@ -415,6 +423,7 @@ struct FmtQ6K {
 // positions (0, 8, 16, 0).
 struct FmtQ80 {
     static constexpr int SBB = 272;
+    static constexpr bool RUNS_OK = false;
     static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) { return 64 * q + i; }
     __host__ __device__ static int xslot(int e4) { return 4 * (e4 & 15) + (e4 >> 4); }
@@ -472,6 +481,7 @@ struct FmtQ80 {
 // j>=4 -> element 32(2q+k) + 16 + 4t + (j-4); positions as Q4_K.
 struct FmtQ40 {
     static constexpr int SBB = 144;
+    static constexpr bool RUNS_OK = false;
     static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) {
         int k = i >> 5, t = (i >> 3) & 3, j = i & 7;

@@ -152,6 +152,26 @@ static bool plan_chunks(StreamParams& p, int budget) {
     using G = ModeGeom<MODE>;
     if (budget < G::ROWS * (Fmt::SBB + 31)) return false;
     const int seg_full = p.nb_seg * Fmt::SBB;
+    // Whole k-segments fit: runs of consecutive rows, one bulk copy each.
+    // A k-segment region holds the tile's rows at their global stride plus
+    // slack for up to four run starts (32 bytes apart), a 16-byte phase and
+    // the 14 bytes a Q6_K lane may read past its super-block.
+    // Rows of 2 KB and more stream at the full rate as separate copies, so
+    // formats whose loads would conflict at the global stride keep padded
+    // per-row slots for them.
+    const int run_piece = align_up(G::ROWS * seg_full, 16) + 144;
+    if (run_piece <= budget && (Fmt::RUNS_OK || seg_full < 2048)) {
+        p.runs = 1;
+        p.n_sbc = 1;
+        p.chunk_ks = budget / run_piece < p.n_kseg ? budget / run_piece : p.n_kseg;
+        p.chunk_sb = p.nb_seg;
+        p.piece_stride = run_piece;
+        p.slot_stride = seg_full;
+        p.stage_bytes = p.chunk_ks * run_piece;
+        p.n_chunk = (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks;
+        return true;
+    }
+    p.runs = 0;
     const int piece_full = align_up(seg_full + 15, 16);
     int nbp_max;
     if (G::ROWS * p.n_kseg * piece_full <= budget) {

@@ -50,8 +50,9 @@ struct StreamParams {
     int chunk_sb;        // groups per k-segment per chunk
     int n_sbc;           // chunks per k-segment (1 => chunks hold whole k-segments)
     int n_chunk;         // chunks per tile
-    int piece_stride;    // smem bytes per (row, k-segment) piece
-    int slot_stride;     // smem bytes per row slot
+    int piece_stride;    // smem bytes per (row, k-segment) piece; runs: per k-segment
+    int slot_stride;     // smem bytes per row slot; runs: the row bytes
+    int runs;            // 1: chunks hold whole rows, copied as runs of consecutive rows
     int stage_bytes;
     int nstages;
     const uint8_t* W0;   // QMV: W; GATEUP: gate; DOWN: down
@@ -264,6 +265,43 @@ __device__ __forceinline__ ChunkDesc chunk_desc(const StreamParams& p, int c) {
     return d;
 }
 
+// Runs: when a chunk holds whole rows (k-segments), the rows of a tile that
+// are consecutive in memory move as one bulk copy.  Row slot r belongs to
+// the run that starts at slot head(r) (run index i: gate 0/1, up 2/3 for the
+// gate/up product, whose units may cross one expert border; 0 otherwise).
+// In a k-segment's region of the stage a run starts at
+// run_dst = align16(head * row_bytes) + 32 * i, and its rows follow at the
+// global row stride, offset by the head row's 16-byte phase.  A bulk copy
+// costs a fixed time in the copy engine whatever its size, so fewer, larger
+// copies are what lets small rows (MoE experts) stream at the HBM rate.
+struct RunSlot {
+    int head, idx;
+};
+
+template <int MODE>
+__device__ __forceinline__ RunSlot run_of(const StreamParams& p, int64_t u0, int s0, int r) {
+    RunSlot rs;
+    if (MODE == MODE_GATEUP) {
+        const int half = r >> 4, j = r & 15;
+        int jb = 16;
+        if (p.moe) {
+            const int64_t b = static_cast<int64_t>(s0 + 1) * p.F - u0;
+            jb = b < 16 ? static_cast<int>(b) : 16;
+        }
+        const int second = j >= jb ? 1 : 0;
+        rs.head = half * 16 + (second ? jb : 0);
+        rs.idx = half * 2 + second;
+    } else {
+        rs.head = 0;
+        rs.idx = 0;
+    }
+    return rs;
+}
+
+__device__ __forceinline__ int run_dst(const StreamParams& p, int head, int idx) {
+    return ((head * p.slot_stride + 15) & ~15) + 32 * idx;
+}
+
 // The stage ring: nstages stages of stage_bytes, a full barrier (one
 // arrival + transaction bytes) and an empty barrier (NCW consumer warps)
 // per stage.  Producer and consumers number chunks with one running count
@@ -301,6 +339,48 @@ __device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int
                 !mbar_wait_bounded(&ring.empty[s], (round - 1) & 1, p.err, DEV_TIMEOUT_EMPTY))
                 return false;
             const ChunkDesc cd = chunk_desc(p, c);
+            if (p.runs) {
+                // copy k: k-segment k / NR, run k % NR (gate/up: 4 runs)
+                constexpr int NR = (MODE == MODE_GATEUP) ? 4 : 1;
+                const int ncopy = NR * cd.nks;
+                const int nrow = static_cast<int>(uend - u0 < G::TU ? uend - u0 : G::TU);
+                uint32_t mine = 0;
+                uintptr_t csrc = 0;
+                uint32_t cbytes = 0;
+                int cdst = 0;
+                if (lane < ncopy) {  // at most 4 * MAX_TOPK / 2 copies: one per lane
+                    const int pk = lane / NR, ri = lane % NR;
+                    int h = 0, e = nrow;  // rows [h, e) of this run
+                    if (MODE == MODE_GATEUP) {
+                        int jb = 16;
+                        if (p.moe) {
+                            const int64_t b = static_cast<int64_t>(s0 + 1) * p.F - u0;
+                            jb = b < 16 ? static_cast<int>(b) : 16;
+                        }
+                        const int lo = (ri & 1) ? jb : 0, hi = (ri & 1) ? 16 : jb;
+                        h = (ri >> 1) * 16 + lo;
+                        e = (ri >> 1) * 16 + (hi < nrow ? hi : nrow);
+                    }
+                    if (e > h) {
+                        const uintptr_t src = reinterpret_cast<uintptr_t>(
+                            row_addr<MODE>(p, s_idx, u0, s0, uend, h, cd.ks0 + pk));
+                        csrc = src & ~uintptr_t(15);
+                        cbytes = static_cast<uint32_t>(
+                            ((src + static_cast<uintptr_t>(e - h) * p.slot_stride + 15) &
+                             ~uintptr_t(15)) - csrc);
+                        cdst = pk * p.piece_stride + run_dst(p, h, ri);
+                        mine = cbytes;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+                if (lane == 0) mbar_arrive_expect_tx(&ring.full[s], mine);
+                __syncwarp();
+                if (cbytes)
+                    bulk_g2s(ring.stages + static_cast<size_t>(s) * ring.stage_bytes + cdst,
+                             reinterpret_cast<const void*>(csrc), cbytes, &ring.full[s], pol);
+                continue;
+            }
             const int ncopy = G::ROWS * cd.nks;
             const uint32_t seg_bytes = static_cast<uint32_t>(cd.nbp * Fmt::SBB);
             uint32_t mine = 0;
@@ -366,11 +446,23 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
         float acc[R];
         // low 32 bits of each row's address (k-segment 0): only the 16-byte
         // phase is needed to find the row inside its staged slot
+        // and the row's offset in a k-segment region of the stage; for runs,
+        // the phase is the run head's and the offset run_dst + rows * stride
         uint32_t rowlo[R];
+        int rowoff[R];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             acc[rr] = 0.f;
-            const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, rr * 8 + g, 0);
+            const int r = rr * 8 + g;
+            int h = r;
+            if (p.runs) {
+                const RunSlot rs = run_of<MODE>(p, u0, s0, r);
+                h = rs.head;
+                rowoff[rr] = run_dst(p, rs.head, rs.idx) + (r - rs.head) * p.slot_stride;
+            } else {
+                rowoff[rr] = r * p.slot_stride;
+            }
+            const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, h, 0);
             rowlo[rr] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a));
             if (MODE == MODE_DOWN && p.moe && a)  // k-segment 0's expert offset removed
                 rowlo[rr] -= static_cast<uint32_t>(s_idx[0]) * static_cast<uint32_t>(p.es0);
@@ -404,8 +496,7 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr) {
                     const int delta = static_cast<int>((rowlo[rr] + ksoff + b0off) & 15u);
-                    sbp[rr] = st + (rr * 8 + g) * p.slot_stride + pk * p.piece_stride + delta +
-                              bb * Fmt::SBB;
+                    sbp[rr] = st + rowoff[rr] + pk * p.piece_stride + delta + bb * Fmt::SBB;
                 }
                 Fmt::template dotR<R>(sbp, q, x, xsg, acc);
             }
