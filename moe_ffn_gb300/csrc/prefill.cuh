@@ -22,6 +22,7 @@
 // k experts are added to the residual with atomics, so their summation order
 // varies from run to run (within the same bound).
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "formats.cuh"
@@ -218,6 +219,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+
 // Byte k of w as the float 0.5 + w.byte_k / 256, built by one byte permute
 // (the byte lands in the mantissa under exponent 2^-1).  Then
 //   fmaf(f, 256 * s, -(128 * s + c)) = s * byte - c
@@ -235,6 +237,11 @@ __device__ __forceinline__ float to_tf32(float v) {
 }
 
 // --------------------------------------------------------- gate / up (f16)
+// The raw Q4_K rows come in by 2-D tensor copies: the gate (up) stack is a
+// [E*F rows][row_bytes] byte tensor, and one box of 144 bytes x 128 rows is
+// super-block b of the item's 128 features, landing as 128 rows of 144 B.
+// Two copies per super-block replace 256 row copies (a copy costs a fixed
+// time in the copy engine).
 // Shared memory: raw Q4_K stages [2][256 rows][144 B]; A/B stages [2] of
 // { A_gate 128x64 f16, A_up 128x64 f16, B 128x64 f16 } (128-byte swizzled
 // K-major tiles, 1024-byte aligned); barriers; TMEM address.
@@ -245,7 +252,9 @@ constexpr int GU_AB_STAGE = 3 * GU_TILE;            // 49,152
 constexpr int PF_META = 96 + 2 * PF_NP * (8 + 4 + 4 + 4);  // barriers + per-pass metadata
 constexpr int GU_SMEM = 1024 + 2 * GU_AB_STAGE + 2 * GU_RAW_STAGE + PF_META;
 
-__global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams p) {
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    pf_gateup_kernel(const PfParams p, const __grid_constant__ CUtensorMap tm_gate,
+                     const __grid_constant__ CUtensorMap tm_up) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -308,16 +317,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gateup_kernel(const PfParams
                                           DEV_PF_TIMEOUT);
                         return;
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(&raw_full[s], GU_RAW_STAGE);
-                    __syncwarp();
-                    for (int r = lane; r < 256; r += 32) {
-                        const uint8_t* m = r < 128 ? p.W0 : p.W1;
-                        const int f = ft * 128 + (r & 127);
-                        const uint8_t* src = m + static_cast<int64_t>(e) * p.es +
-                                             static_cast<int64_t>(f) * p.rb + b * GU_RAW_ROW;
-                        bulk_g2s(raw + s * GU_RAW_STAGE + r * GU_RAW_ROW, src, GU_RAW_ROW,
-                                 &raw_full[s], pol);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&raw_full[s], GU_RAW_STAGE);
+                        const int y = e * p.F + ft * 128;  // first feature row of the item
+                        tma_load_2d(raw + s * GU_RAW_STAGE, &tm_gate, b * GU_RAW_ROW, y,
+                                    &raw_full[s], pol);
+                        tma_load_2d(raw + s * GU_RAW_STAGE + 128 * GU_RAW_ROW, &tm_up,
+                                    b * GU_RAW_ROW, y, &raw_full[s], pol);
                     }
+                    __syncwarp();
                 }
             }
         }
@@ -525,14 +533,15 @@ done:
 }
 
 // ------------------------------------------------------------- down (tf32)
-// Shared memory: raw Q6_K stages [2][128 rows][240 B] (16-byte-aligned copies
-// of each 210-byte super-block); A/B stages [2] of { A 128x32 tf32, B
-// 128x32 tf32 } swizzled; barriers; TMEM address.
-constexpr int DN_RAW_ROW = 240;
-constexpr int DN_RAW_STAGE = 128 * DN_RAW_ROW;      // 30,720
+// Shared memory: A/B stages [2] of { A 128x32 tf32, B 128x32 tf32 } swizzled;
+// the raw Q6_K rows of one (expert, 128-row) tile, all of F, as they lie in
+// memory (the 128 rows are consecutive, so one bulk copy moves them);
+// barriers; TMEM address.  F <= PF_DN_MAX_F.
+constexpr int PF_DN_MAX_F = 1280;
+constexpr int DN_RAW_MAX = 128 * (PF_DN_MAX_F / 256) * 210 + 32;  // 134,432
 constexpr int DN_TILE = 128 * 128;                  // 16,384
 constexpr int DN_AB_STAGE = 2 * DN_TILE;            // 32,768
-constexpr int DN_SMEM = 1024 + 2 * DN_AB_STAGE + 2 * DN_RAW_STAGE + PF_META;
+constexpr int DN_SMEM = 1024 + 2 * DN_AB_STAGE + DN_RAW_MAX + PF_META;
 
 __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -540,9 +549,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ab = base;
     uint8_t* raw = base + 2 * DN_AB_STAGE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + 2 * DN_RAW_STAGE);
-    uint64_t* raw_full = bars + 0;
-    uint64_t* raw_empty = bars + 2;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + DN_RAW_MAX);
+    uint64_t* raw_full = bars + 0;   // [1] used
+    uint64_t* raw_empty = bars + 2;  // [1] used
     uint64_t* ab_full = bars + 4;
     uint64_t* ab_empty = bars + 6;
     uint64_t* acc_full = bars + 8;
@@ -553,7 +562,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int MT = p.H / 128;              // row tiles per expert
-    const int NB = p.F / 256;              // super-blocks per row
     const int items = p.E * MT;
 
     if (warp == 1) umma::tmem_alloc(tmem_slot, 128);
@@ -576,52 +584,34 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
     pdl_trigger();
 
     if (warp == 0) {
+        // one bulk copy per tile: the item's 128 consecutive rows, all of F
         const uint64_t pol = policy_evict_first();
+        const int64_t tile_bytes = 128 * p.rb;
         int rit = 0;
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
             const int e = item / MT, mt = item % MT;
             const int n = __ldcg(p.cnt + e);
             if (n == 0) continue;
-            const int passes = (n + PF_NP - 1) / PF_NP;
-            for (int pass = 0; pass < passes; ++pass) {
-                for (int b = 0; b < NB; ++b, ++rit) {
-                    const int s = rit & 1, round = rit >> 1;
-                    if (round > 0 && !mbar_wait_bounded(&raw_empty[s], (round - 1) & 1, p.err,
-                                                        DEV_PF_TIMEOUT)) {
-                        // the stage's earlier copies completed (its consumers released
-                        // nothing further); wait for the other stage's copies, then leave
-                        mbar_wait_bounded(&raw_full[(s + 1) & 1], ((rit - 1) >> 1) & 1, p.err,
-                                          DEV_PF_TIMEOUT);
-                        return;
-                    }
-                    // per-row 16-byte-aligned windows around each 210-byte block
-                    uint32_t mine = 0;
-                    for (int r = lane; r < 128; r += 32) {
-                        const uintptr_t src = reinterpret_cast<uintptr_t>(
-                            p.W0 + static_cast<int64_t>(e) * p.es +
-                            static_cast<int64_t>(mt * 128 + r) * p.rb + b * 210);
-                        const uintptr_t lo = src & ~uintptr_t(15);
-                        mine += static_cast<uint32_t>(((src + 210 + 15) & ~uintptr_t(15)) - lo);
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-                    if (lane == 0) mbar_arrive_expect_tx(&raw_full[s], mine);
-                    __syncwarp();
-                    for (int r = lane; r < 128; r += 32) {
-                        const uintptr_t src = reinterpret_cast<uintptr_t>(
-                            p.W0 + static_cast<int64_t>(e) * p.es +
-                            static_cast<int64_t>(mt * 128 + r) * p.rb + b * 210);
-                        const uintptr_t lo = src & ~uintptr_t(15);
-                        const uint32_t nbytes =
-                            static_cast<uint32_t>(((src + 210 + 15) & ~uintptr_t(15)) - lo);
-                        bulk_g2s(raw + s * DN_RAW_STAGE + r * DN_RAW_ROW,
-                                 reinterpret_cast<const void*>(lo), nbytes, &raw_full[s], pol);
-                    }
-                }
+            if (rit > 0 &&
+                !mbar_wait_bounded(&raw_empty[0], (rit - 1) & 1, p.err, DEV_PF_TIMEOUT)) {
+                // the previous copy still completes; wait for it, then leave
+                mbar_wait_bounded(&raw_full[0], (rit - 1) & 1, p.err, DEV_PF_TIMEOUT);
+                return;
             }
+            if (lane == 0) {
+                const uintptr_t src = reinterpret_cast<uintptr_t>(
+                    p.W0 + static_cast<int64_t>(e) * p.es + static_cast<int64_t>(mt) * tile_bytes);
+                const uintptr_t lo = src & ~uintptr_t(15);
+                const uint32_t nbytes = static_cast<uint32_t>(
+                    ((src + static_cast<uintptr_t>(tile_bytes) + 15) & ~uintptr_t(15)) - lo);
+                mbar_arrive_expect_tx(&raw_full[0], nbytes);
+                bulk_g2s(raw, reinterpret_cast<const void*>(lo), nbytes, &raw_full[0], pol);
+            }
+            __syncwarp();
+            ++rit;
         }
-        for (int k = rit - 2; k < rit; ++k)
-            if (k >= 0) mbar_wait_bounded(&raw_full[k & 1], (k >> 1) & 1, p.err, DEV_PF_TIMEOUT);
+        // never leave with a copy in flight
+        if (rit > 0) mbar_wait_bounded(&raw_full[0], (rit - 1) & 1, p.err, DEV_PF_TIMEOUT);
         return;
     }
     if (warp == 1) {
@@ -678,6 +668,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
         if (n == 0) continue;
         const int passes = (n + PF_NP - 1) / PF_NP;
         const int32_t* lst = p.list + static_cast<int64_t>(e) * p.T;
+        // this tile's rows (all of F) arrive in one copy
+        if (!mbar_wait_bounded(&raw_full[0], rit & 1, p.err, DEV_PF_TIMEOUT)) goto done;
+        const uint8_t* tile = raw + static_cast<uint32_t>(
+            reinterpret_cast<uintptr_t>(p.W0 + static_cast<int64_t>(e) * p.es +
+                                        static_cast<int64_t>(mt) * 128 * p.rb) & 15u);
         for (int pass = 0; pass < passes; ++pass, ++acc_round) {
             const int nt = min(PF_NP, n - pass * PF_NP);
             const int np = (nt + 15) & ~15;
@@ -689,37 +684,39 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
                 mt_act[wt] = static_cast<int64_t>(pair) * p.F;
             }
             named_bar(2, PF_WORKERS * 32);
-            for (int kc = 0; kc < p.F / 32; ++kc, ++kit) {
+            // B: activations a[pair][kc*32 .. +32].  Each chunk's loads are
+            // issued one chunk ahead, so their L2 latency hides behind the
+            // previous chunk's A decode; rounded to tf32 when stored.
+            constexpr int NBV = PF_NP * 8 / 256;
+            const int KC = p.F / 32;
+            float4 bv[NBV];
+#pragma unroll
+            for (int k = 0; k < NBV; ++k) {
+                const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
+                bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < nt)
+                    bv[k] = __ldcg(reinterpret_cast<const float4*>(p.a + mt_act[j] + ch * 4));
+            }
+            for (int kc = 0; kc < KC; ++kc, ++kit) {
                 const int s = kit & 1, round = kit >> 1;
                 if (round > 0 &&
                     !mbar_wait_bounded(&ab_empty[s], (round - 1) & 1, p.err, DEV_PF_TIMEOUT))
                     goto done;
                 uint8_t* st = ab + s * DN_AB_STAGE;
-                // B: activations a[pair][kc*32 .. +32]; loads issued now, rounded
-                // to tf32 and stored after the A decode below
-                float4 bv[PF_NP * 8 / 256];
+                float4 bn[NBV];  // chunk kc + 1
 #pragma unroll
-                for (int k = 0; k < PF_NP * 8 / 256; ++k) {
+                for (int k = 0; k < NBV; ++k) {
                     const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
-                    bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (j < nt)
-                        bv[k] = __ldcg(reinterpret_cast<const float4*>(p.a + mt_act[j] + kc * 32 +
-                                                                       ch * 4));
+                    bn[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (j < nt && kc + 1 < KC)
+                        bn[k] = __ldcg(reinterpret_cast<const float4*>(p.a + mt_act[j] +
+                                                                       (kc + 1) * 32 + ch * 4));
                 }
                 // A: row r = wt/2, 16 values (half hh) of the 32-element chunk
                 const int sbk = kc & 7;            // chunk within the super-block
-                if (sbk == 0) {
-                    const int rs = rit & 1, rround = rit >> 1;
-                    if (!mbar_wait_bounded(&raw_full[rs], rround & 1, p.err, DEV_PF_TIMEOUT))
-                        goto done;
-                }
                 {
-                    const int rs = rit & 1;
                     const int r = wt >> 1, hh = wt & 1;
-                    const uintptr_t src = reinterpret_cast<uintptr_t>(
-                        p.W0 + static_cast<int64_t>(e) * p.es +
-                        static_cast<int64_t>(mt * 128 + r) * p.rb + (kc >> 3) * 210);
-                    const uint8_t* sb = raw + rs * DN_RAW_STAGE + r * DN_RAW_ROW + (src & 15u);
+                    const uint8_t* sb = tile + static_cast<int64_t>(r) * p.rb + (kc >> 3) * 210;
                     // chunk sbk = (half h, quarter t) of the super-block: elements
                     // 128h + 32t + l, l in [16hh, 16hh + 16)
                     const int h = sbk >> 2, t = sbk & 3;
@@ -753,7 +750,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < PF_NP * 8 / 256; ++k) {
+                for (int k = 0; k < NBV; ++k) {
                     const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
                     if (j < np) {
                         float4 w = bv[k];
@@ -763,11 +760,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
                         w.w = to_tf32(w.w);
                         *reinterpret_cast<float4*>(st + DN_TILE + umma::sw128_offset(j, ch * 16)) = w;
                     }
+                    bv[k] = bn[k];
                 }
-                if (sbk == 7) {
+                if (pass == passes - 1 && kc == KC - 1) {
+                    // the tile's last chunk is decoded: its rows may be replaced
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&raw_empty[rit & 1]);
-                    ++rit;
+                    if (lane == 0) mbar_arrive(&raw_empty[0]);
                 }
                 umma::fence_async_smem();
                 __syncwarp();
@@ -794,6 +792,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
         }
+        ++rit;
     }
 done:
     // the allocating warp frees tensor memory once every worker is past its

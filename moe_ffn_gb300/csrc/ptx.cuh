@@ -100,6 +100,19 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// 2-D tiled TMA load of the box at (x, y) of the tensor map `tmap` (the
+// address of a __grid_constant__ kernel parameter) into shared memory,
+// completing `bar`'s transaction bytes.  x times the element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // Named barrier that also ANDs a flag over its participating threads.
 __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
     uint32_t r;

@@ -1,6 +1,7 @@
 // qmoe.cu — C-ABI entry points of libqmoe.so: argument validation, launch
 // planning and programmatic-dependent launches of the sm_103a kernels.
 // See include/qmoe.h for the contract of every function.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -576,7 +577,8 @@ constexpr int PF_MIN_TOKENS = 32;
 
 static bool prefill_path(const qmoe_moe_shape* s) {
     return s->n_tokens >= PF_MIN_TOKENS && s->gate_qtype == QT_Q4_K && s->up_qtype == QT_Q4_K &&
-           s->down_qtype == QT_Q6_K && s->expert_dim % 256 == 0 && s->hidden % 256 == 0;
+           s->down_qtype == QT_Q6_K && s->expert_dim % 256 == 0 && s->hidden % 256 == 0 &&
+           s->expert_dim <= pf::PF_DN_MAX_F;
 }
 
 // Prefill workspace carve-up (byte offsets from ws).
@@ -612,6 +614,45 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* s) {
         return pf > decode ? pf : decode;
     }
     return decode;
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link
+// against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// A [rows][row_bytes] byte matrix as a 2-D tensor map with boxes of
+// box_bytes x box_rows.  row_bytes, box_bytes and the base must be multiples
+// of 16 bytes.
+static qmoe_status rows_map(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows,
+                            uint32_t box_bytes, uint32_t box_rows) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return fail(QMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {box_bytes, box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QMOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return QMOE_OK;
 }
 
 static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
@@ -661,8 +702,16 @@ static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
     pg.residual = residual;
     pg.err = d.err;
     const int items_gu = E * (F / 128);
+    CUtensorMap tm_gate, tm_up;
+    if (qmoe_status r = rows_map(&tm_gate, gate_stack, pg.rb, static_cast<int64_t>(E) * F,
+                                 pf::GU_RAW_ROW, 128))
+        return r;
+    if (qmoe_status r = rows_map(&tm_up, up_stack, pg.rb, static_cast<int64_t>(E) * F,
+                                 pf::GU_RAW_ROW, 128))
+        return r;
     e = launch_pdl(pf::pf_gateup_kernel, dim3(items_gu < d.sms ? items_gu : d.sms),
-                   dim3(pf::PF_THREADS), static_cast<size_t>(pf::GU_SMEM), st, pg);
+                   dim3(pf::PF_THREADS), static_cast<size_t>(pf::GU_SMEM), st, pg, tm_gate,
+                   tm_up);
     if (e != cudaSuccess) return cuda_fail(e, "pf_gateup launch");
     pf::PfParams pd = pg;
     pd.W0 = static_cast<const uint8_t*>(down_stack);
