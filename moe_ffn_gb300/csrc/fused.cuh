@@ -174,8 +174,9 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t cta = blockIdx.x, ncta = gridDim.x;
-    const int64_t gb = f.gu.units * cta / ncta, ge = f.gu.units * (cta + 1) / ncta;
-    const int64_t db = f.dn.units * cta / ncta, de = f.dn.units * (cta + 1) / ncta;
+    int64_t gb, ge, db, de;
+    unit_range(f.gu, static_cast<int>(cta), gb, ge);
+    unit_range(f.dn, static_cast<int>(cta), db, de);
     constexpr int NC = NCW * 32;  // consumer threads
 
     if (tid == NC) {

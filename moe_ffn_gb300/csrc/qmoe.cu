@@ -208,19 +208,30 @@ static bool plan_chunks(StreamParams& p, int budget) {
 // Plan chunking and pipeline depth for a streamed GEMV; false if it cannot
 // fit in shared memory.
 template <class Fmt, int MODE>
-static bool plan(StreamParams& p, int smem_optin, int* smem_bytes) {
-    // stage budget: at most 96 KB, and at least two stages must fit beside
-    // the x' table
+static bool plan(StreamParams& p, int smem_optin, int grid, int* smem_bytes) {
+    using G = ModeGeom<MODE>;
     p.stage_bytes = 0;
     p.nstages = 0;
     const int room = smem_optin - smem_layout(p).total;
-    const int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
-    if (!plan_chunks<Fmt, MODE>(p, budget)) return false;
+    // A CTA with a single tile gains nothing from a ring: one stage may then
+    // hold the whole tile (whole rows, so few and large copies).  Otherwise
+    // the stage budget is at most 96 KB, and two stages must fit beside the
+    // x' table.
+    const int64_t per_cta = (p.units + grid - 1) / grid;
+    const bool one_tile = per_cta <= G::TU;
+    bool planned = false;
+    if (one_tile) {
+        planned = plan_chunks<Fmt, MODE>(p, room) && p.n_chunk == 1;
+    }
+    if (!planned) {
+        const int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
+        if (!plan_chunks<Fmt, MODE>(p, budget)) return false;
+    }
     p.nstages = 0;
     const int fixed = smem_layout(p).total;
     int ns = (smem_optin - fixed) / p.stage_bytes;
     if (ns > MAX_STAGES) ns = MAX_STAGES;
-    if (ns < 2) return false;
+    if (ns < (planned ? 1 : 2)) return false;
     p.nstages = ns;
     *smem_bytes = smem_layout(p).total;
     return true;
@@ -229,7 +240,10 @@ static bool plan(StreamParams& p, int smem_optin, int* smem_bytes) {
 template <class Fmt, int MODE>
 static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st) {
     int smem = 0;
-    if (!plan<Fmt, MODE>(p, d.smem_optin, &smem))
+    const int64_t grid = p.units < d.sms ? p.units : d.sms;
+    p.uq = p.units / grid;
+    p.ur = static_cast<int>(p.units % grid);
+    if (!plan<Fmt, MODE>(p, d.smem_optin, static_cast<int>(grid), &smem))
         return fail(QMOE_ERR_UNSUPPORTED,
                     "K = %d x %d groups of 256 does not fit the shared-memory pipeline",
                     p.n_kseg, p.nb_seg);
@@ -243,7 +257,6 @@ static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st)
         configured_smem[dev & 63] = smem;
     }
     p.err = d.err;
-    const int64_t grid = p.units < d.sms ? p.units : d.sms;
     cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NTHREADS),
                                static_cast<size_t>(smem), st, p);
     if (e != cudaSuccess) return cuda_fail(e, "stream_gemv launch");
@@ -306,6 +319,10 @@ static int run_fused(FusedParams f, const DevInfo& d, cudaStream_t st, qmoe_stat
         configured_smem[dev & 63] = smem;
     }
     f.err = f.gu.err = f.dn.err = d.err;
+    f.gu.uq = f.gu.units / d.sms;
+    f.gu.ur = static_cast<int>(f.gu.units % d.sms);
+    f.dn.uq = f.dn.units / d.sms;
+    f.dn.ur = static_cast<int>(f.dn.units % d.sms);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(d.sms));
     cfg.blockDim = dim3(NTHREADS);

@@ -44,6 +44,8 @@ enum Mode : int { MODE_QMV = 0, MODE_GATEUP = 1, MODE_DOWN = 2 };
 
 struct StreamParams {
     int64_t units;       // output units: rows (QMV, DOWN) or gate/up row pairs (GATEUP)
+    int64_t uq;          // units per CTA, rounded down (units / grid)
+    int ur;              // CTAs that take one more unit (units % grid)
     int nb_seg;          // 256-element groups per k-segment
     int n_kseg;          // k-segments: 1, or top_k for the MoE down product
     int chunk_ks;        // whole k-segments per chunk (when n_sbc == 1)
@@ -243,6 +245,14 @@ __device__ __forceinline__ const uint8_t* row_addr(const StreamParams& p, const 
     // DOWN
     if (p.moe) return p.W0 + static_cast<int64_t>(s_idx[ks]) * p.es0 + u * p.rb0;
     return p.W0 + u * p.rb0;
+}
+
+// The units [beg, end) of CTA `cta`: an even split, the first ur CTAs one
+// unit larger (quotient and remainder come from the host).
+__device__ __forceinline__ void unit_range(const StreamParams& p, int cta, int64_t& beg,
+                                           int64_t& end) {
+    beg = p.uq * cta + (cta < p.ur ? cta : p.ur);
+    end = beg + p.uq + (cta < p.ur ? 1 : 0);
 }
 
 struct ChunkDesc {
@@ -568,8 +578,8 @@ __global__ void __launch_bounds__(NTHREADS) stream_gemv_kernel(const StreamParam
     float* xq = reinterpret_cast<float*>(smem + L.off_xq);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t cta = blockIdx.x, ncta = gridDim.x;
-    const int64_t ubeg = p.units * cta / ncta, uend = p.units * (cta + 1) / ncta;
+    int64_t ubeg, uend;
+    unit_range(p, static_cast<int>(blockIdx.x), ubeg, uend);
 
     // The producer's lane 0 initialises the stage barriers.  Without routing
     // the producer starts streaming at once and only arrives on named
