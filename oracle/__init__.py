@@ -79,6 +79,8 @@ def _load():
                                            P, P, P, P, P, P, P]
             lib.orc_row_bytes.restype = i64
             lib.orc_row_bytes.argtypes = [ctypes.c_int, i64]
+            lib.orc_rmsnorm.restype = ctypes.c_int
+            lib.orc_rmsnorm.argtypes = [P, P, i64, ctypes.c_double, P]
             _lib = lib
     return _lib
 
@@ -211,3 +213,20 @@ def ffn_swiglu(gate_qt, up_qt, down_qt, hidden, inter, gate, up, down, x, residu
     if rc != 0:
         raise ValueError("orc_ffn_swiglu rejected the shape")
     return out, tol
+
+
+def rmsnorm(h, w, eps: float) -> np.ndarray:
+    """ffn_norm: h * w / sqrt(mean(h^2) + eps) per row of h ([T][n] or [n]),
+    in double (orc_rmsnorm)."""
+    h = np.ascontiguousarray(h, dtype=np.float32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n = w.shape[0]
+    rows = h.reshape(-1, n)
+    out = np.zeros(rows.shape, np.float64)
+    for t in range(rows.shape[0]):
+        r = np.ascontiguousarray(rows[t])
+        o = np.zeros(n, np.float64)
+        if _load().orc_rmsnorm(_ptr(r), _ptr(w), n, float(eps), _ptr(o)) != 0:
+            raise ValueError("orc_rmsnorm rejected the arguments")
+        out[t] = o
+    return out.reshape(h.shape)

@@ -16,6 +16,7 @@
  *   [aprender qwen3 moe] "aprender-serve 0.70.2 —
  *       forward_qwen3_moe_resident.rs": module doc (op order, "Kernels"),
  *       ExpertStack::expert, moe_layer, last_routes.
+ *   [ferrox gpu.rs] also gives FUSED_ADD_RMSNORM_KERNEL_SRC (ffn_norm).
  *
  * Precision: block values are formed in f32 in the order the page kernels
  * write them; every dot product and every MoE intermediate is carried in
@@ -333,6 +334,21 @@ int orc_route(const double *logits, int E, int k, int32_t *idx, double *w) {
     for (int i = 0; i < k; i++) { idx[i] = order[i]; w[i] = p[order[i]] / s; }
     free(p);
     free(order);
+    return 0;
+}
+
+/* ------------------------------ ffn_norm -------------------------------
+ * RMSNorm as FUSED_ADD_RMSNORM_KERNEL_SRC in [ferrox gpu.rs] writes it,
+ * applied to the hidden state alone (moe_layer in [aprender qwen3 moe] norms
+ * `hidden` with ffn_norm before the router):
+ *   out[i] = h[i] * w[i] / sqrt(mean_j h[j]^2 + eps).
+ * Carried in double. */
+int orc_rmsnorm(const float *h, const float *w, int64_t n, double eps, double *out) {
+    if (n <= 0 || eps < 0.0) return -1;
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; i++) ss += (double)h[i] * (double)h[i];
+    const double denom = sqrt(ss / (double)n + eps);
+    for (int64_t i = 0; i < n; i++) out[i] = (double)h[i] * (double)w[i] / denom;
     return 0;
 }
 
