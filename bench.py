@@ -360,7 +360,19 @@ def bench_layers(qm, synth, dev, stream, args):
                          "launches_per_token": layer_launches(3),
                          "launch": f"CUDA graph of {n} tokens",
                          "workload": "hidden 2048, 128 experts, top-8, expert_dim 768, Q4_K/Q4_K/Q6_K"}
-    del d, inp, gm
+    # the same layer with ffn_norm fused in front (input = the hidden state)
+    nw = torch.from_numpy(synth.norm_weight(synth.rng(98), shp["hidden"])).to(dev)
+    hpool = xpool.clone()
+    wsn = torch.zeros(qm.moe_ffn_rmsnorm_workspace_size(s), dtype=torch.uint8, device=dev)
+
+    def ncall(i):
+        qm.moe_ffn_rmsnorm(d["router"], d["gate"], d["up"], d["down"], s, nw, 1e-6,
+                           hpool[i % 64], idx, None, wsn)
+    gn = capture(torch, ncall, n)
+    gn.replay()
+    usn = time_replays(torch, gn, reps) * 1e3 / (reps * n)
+    out["moe_decode"]["us_per_token_with_ffn_norm"] = round(usn, 3)
+    del d, inp, gm, gn
     torch.cuda.empty_cache()
 
     # dense SwiGLU FFN: 114 MB weights, 5 copies rotating (> 4x L2)

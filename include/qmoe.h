@@ -131,6 +131,30 @@ qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int g
                        int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
                        const float* x, float* residual, void* ws, size_t ws_bytes, void* stream);
 
+/* Bytes of workspace ffn_swiglu_rmsnorm needs: ffn_swiglu's plus room for the
+ * normed input. */
+size_t ffn_swiglu_rmsnorm_workspace_size(int64_t hidden, int64_t inter);
+
+/* ffn_swiglu with ffn_norm in front, on the hidden state itself:
+ *   residual += down( silu(gate xn) * (up xn) ),
+ *   xn = residual * norm_w / sqrt(mean(residual^2) + eps)
+ * — the RMSNorm of FUSED_ADD_RMSNORM_KERNEL_SRC on "ferrox-cuda 0.14.0 —
+ * src/gpu.rs" (without its add), applied before the FFN as moe_layer on
+ * "aprender-serve 0.70.2 — forward_qwen3_moe_resident.rs" norms `hidden`
+ * with ffn_norm.
+ *   norm_w     [hidden] f32, 16-byte aligned (the ffn_norm weight)
+ *   eps        finite, >= 0
+ *   residual   [hidden] f32, 16-byte aligned: the layer's input, updated in
+ *              place with the FFN output
+ *   ws         >= ffn_swiglu_rmsnorm_workspace_size bytes, 16-byte aligned
+ * Other arguments, rules and errors as ffn_swiglu.  The fused layer kernel
+ * computes the norm itself (no extra launch); the two-kernel form runs a
+ * norm kernel first. */
+qmoe_status ffn_swiglu_rmsnorm(const void* gate, const void* up, const void* down,
+                               int gate_qtype, int up_qtype, int down_qtype, int64_t hidden,
+                               int64_t inter, const float* norm_w, float eps, float* residual,
+                               void* ws, size_t ws_bytes, void* stream);
+
 /* Bytes of workspace moe_ffn needs for this shape (256 bytes of grid-barrier
  * state, then the logits, activations and, for many tokens, the grouping
  * buffers). */
@@ -167,6 +191,28 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
                     const void* down_stack, const qmoe_moe_shape* shape, const float* x,
                     float* residual, int32_t* topk_idx, float* topk_w, void* ws,
                     size_t ws_bytes, void* stream);
+
+/* Bytes of workspace moe_ffn_rmsnorm needs: moe_ffn's plus [T][H] f32 for the
+ * normed inputs. */
+size_t moe_ffn_rmsnorm_workspace_size(const qmoe_moe_shape* shape);
+
+/* moe_ffn with ffn_norm in front, on each token's hidden state:
+ *   xn_t = residual_t * norm_w / sqrt(mean(residual_t^2) + eps)
+ *   residual_t += MoE(xn_t)       (router, routing and experts as moe_ffn)
+ * — moe_layer on "aprender-serve 0.70.2 — forward_qwen3_moe_resident.rs"
+ * from rmsnorm_into(hidden, ffn_norm) on, the norm as
+ * FUSED_ADD_RMSNORM_KERNEL_SRC on "ferrox-cuda 0.14.0 — src/gpu.rs" computes
+ * it without its add.
+ *   norm_w      [H] f32, 16-byte aligned;  eps finite, >= 0
+ *   residual    [T][H] f32, 16-byte aligned: the input, updated in place
+ *   ws          >= moe_ffn_rmsnorm_workspace_size(shape) bytes
+ * Other arguments, rules and errors as moe_ffn (there is no x).  The
+ * per-token fused kernel norms its input itself; the tensor-core and
+ * separate-kernel forms run a norm kernel first. */
+qmoe_status moe_ffn_rmsnorm(const float* router_W, const void* gate_stack, const void* up_stack,
+                            const void* down_stack, const qmoe_moe_shape* shape,
+                            const float* norm_w, float eps, float* residual, int32_t* topk_idx,
+                            float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
 /* Bytes of the built-in scratch used by moe_ffn_noalloc. */
 #define QMOE_NOALLOC_SCRATCH_BYTES (1u << 20)

@@ -87,6 +87,13 @@ SIGNATURES = {
                                ctypes.c_size_t, _P]),
     "moe_ffn_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(_Shape), _P, _P, _P, _P,
                                         _P]),
+    "ffn_swiglu_rmsnorm_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
+    "ffn_swiglu_rmsnorm": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          _I64, _I64, _P, ctypes.c_float, _P, _P, ctypes.c_size_t,
+                                          _P]),
+    "moe_ffn_rmsnorm_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(_Shape)]),
+    "moe_ffn_rmsnorm": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(_Shape), _P, ctypes.c_float,
+                                       _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qmoe_device_status": (ctypes.c_int, [_P]),
     "qmoe_last_error": (ctypes.c_char_p, []),
     "qmoe_row_bytes": (_I64, [ctypes.c_int, _I64]),
@@ -176,6 +183,36 @@ def moe_ffn(router_W, gate_stack, up_stack, down_stack, shape: _Shape, x, residu
     _check(lib().moe_ffn(_ptr(router_W), _ptr(gate_stack), _ptr(up_stack), _ptr(down_stack),
                          ctypes.byref(shape), _ptr(x), _ptr(residual), _ptr(topk_idx),
                          _ptr(topk_w), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def ffn_swiglu_rmsnorm_workspace_size(hidden: int, inter: int) -> int:
+    return int(lib().ffn_swiglu_rmsnorm_workspace_size(hidden, inter))
+
+
+def ffn_swiglu_rmsnorm(gate, up, down, gate_qtype, up_qtype, down_qtype, hidden, inter, norm_w,
+                       eps, residual, ws, ws_bytes=None, stream=None) -> None:
+    """residual += FFN(rmsnorm(residual)) (see include/qmoe.h)."""
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size()
+    _check(lib().ffn_swiglu_rmsnorm(_ptr(gate), _ptr(up), _ptr(down), gate_qtype, up_qtype,
+                                    down_qtype, hidden, inter, _ptr(norm_w), float(eps),
+                                    _ptr(residual), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_ffn_rmsnorm_workspace_size(shape: _Shape) -> int:
+    return int(lib().moe_ffn_rmsnorm_workspace_size(ctypes.byref(shape)))
+
+
+def moe_ffn_rmsnorm(router_W, gate_stack, up_stack, down_stack, shape: _Shape, norm_w, eps,
+                    residual, topk_idx=None, topk_w=None, ws=None, ws_bytes=None,
+                    stream=None) -> None:
+    """residual_t += MoE(rmsnorm(residual_t)) for every token (see include/qmoe.h)."""
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size()
+    _check(lib().moe_ffn_rmsnorm(_ptr(router_W), _ptr(gate_stack), _ptr(up_stack),
+                                 _ptr(down_stack), ctypes.byref(shape), _ptr(norm_w), float(eps),
+                                 _ptr(residual), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws_bytes,
+                                 _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 1 << 20

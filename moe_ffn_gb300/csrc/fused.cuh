@@ -41,6 +41,8 @@ struct FusedParams {
     int moe, E, H, topk;
     int32_t* topk_idx_out;    // nullable
     float* topk_w_out;        // nullable
+    const float* norm_w;      // nullable: ffn_norm weight [H]; gu.x is then the hidden state
+    float eps;
     unsigned* err;
 };
 
@@ -95,7 +97,7 @@ __device__ __forceinline__ void sync_invalidate(unsigned long long* sync) {
 }
 
 // By one thread per CTA, after the dependency wait.  False on a timeout.
-__device__ bool sync_open(unsigned long long* sync, unsigned* err) {
+__device__ __forceinline__ bool sync_open(unsigned long long* sync, unsigned* err) {
     if (ld_acquire_u64(sync + SYNC_TAG) == SYNC_VALID) return true;
     if (blockIdx.x == 0) {
         sync[SYNC_ARRIVE] = 0;
@@ -119,7 +121,7 @@ __device__ bool sync_open(unsigned long long* sync, unsigned* err) {
 // release, the wait an acquire (no full fence: one would also wait for the
 // producer's copies in flight).  False if the other CTAs did not arrive
 // within ~2 s.
-__device__ bool grid_barrier(unsigned long long* sync, unsigned n, unsigned* err) {
+__device__ __forceinline__ bool grid_barrier(unsigned long long* sync, unsigned n, unsigned* err) {
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(sync + SYNC_ARRIVE) : "memory");
     const unsigned long long target = static_cast<unsigned long long>(n) * gridDim.x;
     const uint64_t t0 = global_ns();
@@ -136,7 +138,7 @@ __device__ bool grid_barrier(unsigned long long* sync, unsigned n, unsigned* err
 
 // By one thread per CTA after its last barrier: the last CTA out leaves the
 // counters at zero for the next call.
-__device__ void sync_close(unsigned long long* sync) {
+__device__ __forceinline__ void sync_close(unsigned long long* sync) {
     unsigned long long old;
     asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;"
                  : "=l"(old)
@@ -209,15 +211,27 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
     pdl_wait();
     pdl_trigger();
     if (tid == 0 && !sync_open(f.sync, f.err)) s_abort = 1;
-    build_xprime<FmtG>(f.gu.x, f.gu.nb_seg, xq, xs, tid, NC);
+    // ffn_norm (optional): every CTA reads the whole hidden state anyway
+    const float inv =
+        f.norm_w ? rms_inverse(f.gu.x, f.gu.nb_seg * 256, f.eps, red, tid, NC, 1) : 1.f;
+    build_xprime<FmtG>(f.gu.x, f.gu.nb_seg, xq, xs, tid, NC, f.norm_w, inv);
     if (f.moe) {
         // logits of this CTA's experts: e = cta, cta + ncta, ...
         const float4* x4 = reinterpret_cast<const float4*>(f.gu.x);
         for (int64_t e = cta; e < f.E; e += ncta) {
             const float4* r4 = reinterpret_cast<const float4*>(f.router + e * f.H);
             float acc = 0.f;
+            const float4* n4 = reinterpret_cast<const float4*>(f.norm_w);
             for (int j = tid; j < f.H / 4; j += NC) {
-                const float4 w = __ldg(r4 + j), xv = __ldcg(x4 + j);
+                const float4 w = __ldg(r4 + j);
+                float4 xv = __ldcg(x4 + j);
+                if (n4) {
+                    const float4 nv = __ldg(n4 + j);
+                    xv.x *= inv * nv.x;
+                    xv.y *= inv * nv.y;
+                    xv.z *= inv * nv.z;
+                    xv.w *= inv * nv.w;
+                }
                 acc = fmaf(w.x, xv.x, acc);
                 acc = fmaf(w.y, xv.y, acc);
                 acc = fmaf(w.z, xv.z, acc);

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdlib>
 #include <cstdio>
@@ -452,6 +453,38 @@ static qmoe_status run_f32_gemv(const float* R, const float* x, float* y, int64_
     return QMOE_OK;
 }
 
+// ffn_norm for T rows of n: out[t] = h[t] * w / sqrt(mean(h[t]^2) + eps), one
+// CTA per row — the fused add+RMSNorm kernel of "ferrox-cuda 0.14.0 —
+// src/gpu.rs" without the add (moe_layer norms the hidden state).  Used in
+// front of the tensor-core and separate-kernel forms; the fused layer
+// kernel norms its input itself.
+constexpr int NORM_THREADS = 256;
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __restrict__ h,
+                                                               const float* __restrict__ w, int n,
+                                                               float eps, float* __restrict__ out) {
+    __shared__ float red[NORM_THREADS / 32];
+    const int64_t off = static_cast<int64_t>(blockIdx.x) * n;
+    pdl_wait();
+    pdl_trigger();
+    const float inv = rms_inverse(h + off, n, eps, red, threadIdx.x, NORM_THREADS, 0);
+    const float4* h4 = reinterpret_cast<const float4*>(h + off);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    float4* o4 = reinterpret_cast<float4*>(out + off);
+    for (int i = threadIdx.x; i < n / 4; i += NORM_THREADS) {
+        const float4 v = __ldcg(h4 + i), wv = __ldg(w4 + i);
+        o4[i] = make_float4(v.x * (inv * wv.x), v.y * (inv * wv.y), v.z * (inv * wv.z),
+                            v.w * (inv * wv.w));
+    }
+}
+
+static qmoe_status run_rmsnorm(const float* h, const float* w, int64_t rows, int64_t n, float eps,
+                               float* out, cudaStream_t st) {
+    cudaError_t e = launch_pdl(rmsnorm_kernel, dim3(static_cast<unsigned>(rows)),
+                               dim3(NORM_THREADS), 0, st, h, w, static_cast<int>(n), eps, out);
+    if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+    return QMOE_OK;
+}
+
 }  // namespace qmoe
 
 using namespace qmoe;
@@ -523,35 +556,42 @@ static qmoe_status check_ffn_qtypes(const char* fn, int gq, int uq, int dq) {
     return QMOE_OK;
 }
 
-qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int gate_qtype,
-                       int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
-                       const float* x, float* residual, void* ws, size_t ws_bytes, void* stream) {
-    g_last_error.clear();
+// Checks shared by ffn_swiglu and ffn_swiglu_rmsnorm.  `x` is the FFN input
+// (ffn_swiglu) or the norm weight (ffn_swiglu_rmsnorm); `need` the workspace.
+static qmoe_status ffn_check(const char* fn, const void* gate, const void* up, const void* down,
+                             int gate_qtype, int up_qtype, int down_qtype, int64_t hidden,
+                             int64_t inter, const float* x, const float* residual, const void* ws,
+                             size_t ws_bytes, size_t need, uintptr_t res_align) {
     if (!gate || !up || !down || !x || !residual || !ws)
-        return fail(QMOE_ERR_INVALID_ARGUMENT, "ffn_swiglu: null pointer");
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: null pointer", fn);
     if (hidden <= 0 || inter <= 0)
-        return fail(QMOE_ERR_INVALID_ARGUMENT, "ffn_swiglu: hidden=%lld inter=%lld must be >= 1",
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: hidden=%lld inter=%lld must be >= 1", fn,
                     (long long)hidden, (long long)inter);
-    if (qmoe_status s = check_ffn_qtypes("ffn_swiglu", gate_qtype, up_qtype, down_qtype)) return s;
+    if (qmoe_status s = check_ffn_qtypes(fn, gate_qtype, up_qtype, down_qtype)) return s;
     if (hidden % block_elems(gate_qtype) || inter % block_elems(down_qtype))
-        return fail(QMOE_ERR_INVALID_ARGUMENT,
-                    "ffn_swiglu: hidden/inter not whole numbers of blocks");
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: hidden/inter not whole numbers of blocks", fn);
     if (hidden % 256 || inter % 256)
-        return fail(QMOE_ERR_UNSUPPORTED, "ffn_swiglu: hidden and inter must be multiples of 256");
+        return fail(QMOE_ERR_UNSUPPORTED, "%s: hidden and inter must be multiples of 256", fn);
     if (hidden > MAX_K || inter > MAX_K)
-        return fail(QMOE_ERR_UNSUPPORTED, "ffn_swiglu: hidden/inter exceed %lld", (long long)MAX_K);
-    if (ws_bytes < ffn_swiglu_workspace_size(hidden, inter))
-        return fail(QMOE_ERR_INVALID_ARGUMENT, "ffn_swiglu: workspace %zu < %zu bytes", ws_bytes,
-                    ffn_swiglu_workspace_size(hidden, inter));
+        return fail(QMOE_ERR_UNSUPPORTED, "%s: hidden/inter exceed %lld", fn, (long long)MAX_K);
+    if (ws_bytes < need)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: workspace %zu < %zu bytes", fn, ws_bytes,
+                    need);
     if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(down, 16) || !aligned(x, 16) ||
-        !aligned(residual, 4) || !aligned(ws, 16))
+        !aligned(residual, res_align) || !aligned(ws, 16))
         return fail(QMOE_ERR_INVALID_ARGUMENT,
-                    "ffn_swiglu: weights, x and ws must be 16-byte aligned");
-    DevInfo* d = nullptr;
-    if (qmoe_status s = device_info(&d)) return s;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + WS_SYNC_BYTES);
+                    "%s: weights, x/norm weight and ws must be 16-byte aligned, residual %d-byte",
+                    fn, static_cast<int>(res_align));
+    return QMOE_OK;
+}
 
+// The dense FFN layer.  With norm_w, the input is ffn_norm(residual) and x is
+// unused; xn is workspace for the normed input of the two-kernel form.
+static qmoe_status ffn_core(const void* gate, const void* up, const void* down, int gate_qtype,
+                            int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
+                            const float* x, const float* norm_w, float eps, float* residual,
+                            void* ws, float* xn, const DevInfo& d, cudaStream_t st) {
+    float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + WS_SYNC_BYTES);
     StreamParams pg = {};
     pg.units = inter;
     pg.nb_seg = static_cast<int>(hidden / 256);
@@ -560,7 +600,7 @@ qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int g
     pg.rb0 = row_bytes_of(gate_qtype, hidden);
     pg.W1 = static_cast<const uint8_t*>(up);
     pg.rb1 = row_bytes_of(up_qtype, hidden);
-    pg.x = x;
+    pg.x = norm_w ? residual : x;
     pg.out = a;
 
     StreamParams pd = {};
@@ -576,12 +616,58 @@ qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int g
     f.gu = pg;
     f.dn = pd;
     f.sync = static_cast<unsigned long long*>(ws);
+    f.norm_w = norm_w;
+    f.eps = eps;
     qmoe_status ferr = QMOE_OK;
-    const int fr = dispatch_fused(gate_qtype, down_qtype, f, *d, st, &ferr);
+    const int fr = dispatch_fused(gate_qtype, down_qtype, f, d, st, &ferr);
     if (fr < 0) return ferr;
     if (fr > 0) return QMOE_OK;
-    if (qmoe_status s = dispatch<MODE_GATEUP>(gate_qtype, pg, *d, st)) return s;
-    return dispatch<MODE_DOWN>(down_qtype, pd, *d, st);
+    if (norm_w) {
+        if (qmoe_status s = run_rmsnorm(residual, norm_w, 1, hidden, eps, xn, st)) return s;
+        pg.x = xn;
+    }
+    if (qmoe_status s = dispatch<MODE_GATEUP>(gate_qtype, pg, d, st)) return s;
+    return dispatch<MODE_DOWN>(down_qtype, pd, d, st);
+}
+
+qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int gate_qtype,
+                       int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
+                       const float* x, float* residual, void* ws, size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (qmoe_status s = ffn_check("ffn_swiglu", gate, up, down, gate_qtype, up_qtype, down_qtype,
+                                  hidden, inter, x, residual, ws, ws_bytes,
+                                  ffn_swiglu_workspace_size(hidden, inter), 4))
+        return s;
+    DevInfo* d = nullptr;
+    if (qmoe_status s = device_info(&d)) return s;
+    return ffn_core(gate, up, down, gate_qtype, up_qtype, down_qtype, hidden, inter, x, nullptr,
+                    0.f, residual, ws, nullptr, *d, static_cast<cudaStream_t>(stream));
+}
+
+size_t ffn_swiglu_rmsnorm_workspace_size(int64_t hidden, int64_t inter) {
+    if (hidden <= 0 || inter <= 0) return 0;
+    return ffn_swiglu_workspace_size(hidden, inter) +
+           static_cast<size_t>(align_up(static_cast<int>(hidden * 4), 256));
+}
+
+qmoe_status ffn_swiglu_rmsnorm(const void* gate, const void* up, const void* down,
+                               int gate_qtype, int up_qtype, int down_qtype, int64_t hidden,
+                               int64_t inter, const float* norm_w, float eps, float* residual,
+                               void* ws, size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (qmoe_status s = ffn_check("ffn_swiglu_rmsnorm", gate, up, down, gate_qtype, up_qtype,
+                                  down_qtype, hidden, inter, norm_w, residual, ws, ws_bytes,
+                                  ffn_swiglu_rmsnorm_workspace_size(hidden, inter), 16))
+        return s;
+    if (!(eps >= 0.f) || !std::isfinite(eps))
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "ffn_swiglu_rmsnorm: eps=%g must be finite, >= 0",
+                    static_cast<double>(eps));
+    DevInfo* d = nullptr;
+    if (qmoe_status s = device_info(&d)) return s;
+    float* xn = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                         ffn_swiglu_workspace_size(hidden, inter));
+    return ffn_core(gate, up, down, gate_qtype, up_qtype, down_qtype, hidden, inter, nullptr,
+                    norm_w, eps, residual, ws, xn, *d, static_cast<cudaStream_t>(stream));
 }
 
 static size_t moe_logits_bytes(const qmoe_moe_shape* s) {
@@ -742,49 +828,64 @@ static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
     return QMOE_OK;
 }
 
-qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* up_stack,
-                    const void* down_stack, const qmoe_moe_shape* shape, const float* x,
-                    float* residual, int32_t* topk_idx, float* topk_w, void* ws,
-                    size_t ws_bytes, void* stream) {
-    g_last_error.clear();
-    if (!shape) return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: null shape");
+// Checks shared by moe_ffn and moe_ffn_rmsnorm.  `x` is the FFN input
+// (moe_ffn) or the norm weight (moe_ffn_rmsnorm); `need` the workspace.
+static qmoe_status moe_check(const char* fn, const float* router_W, const void* gate_stack,
+                             const void* up_stack, const void* down_stack,
+                             const qmoe_moe_shape* shape, const float* x, const float* residual,
+                             const void* ws, size_t ws_bytes, size_t need, uintptr_t res_align) {
+    if (!shape) return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: null shape", fn);
     const qmoe_moe_shape s = *shape;
     if (!router_W || !gate_stack || !up_stack || !down_stack || !x || !residual || !ws)
-        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: null pointer");
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: null pointer", fn);
     // check_moe_shape: every count positive, k <= E
     if (s.hidden <= 0 || s.expert_dim <= 0 || s.num_experts <= 0 || s.top_k <= 0 ||
         s.n_tokens <= 0)
         return fail(QMOE_ERR_INVALID_ARGUMENT,
-                    "moe_ffn: incomplete MoE shape (hidden=%d expert_dim=%d num_experts=%d "
-                    "top_k=%d n_tokens=%d)",
+                    "%s: incomplete MoE shape (hidden=%d expert_dim=%d num_experts=%d "
+                    "top_k=%d n_tokens=%d)", fn,
                     s.hidden, s.expert_dim, s.num_experts, s.top_k, s.n_tokens);
     if (s.top_k > s.num_experts)
-        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: top_k=%d > num_experts=%d", s.top_k,
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: top_k=%d > num_experts=%d", fn, s.top_k,
                     s.num_experts);
-    if (qmoe_status st = check_ffn_qtypes("moe_ffn", s.gate_qtype, s.up_qtype, s.down_qtype))
+    if (qmoe_status st = check_ffn_qtypes(fn, s.gate_qtype, s.up_qtype, s.down_qtype))
         return st;
     if (s.num_experts > MAX_EXPERTS || s.top_k > MAX_TOPK)
         return fail(QMOE_ERR_UNSUPPORTED,
-                    "moe_ffn: on-device routing supports num_experts <= %d and top_k <= %d",
+                    "%s: on-device routing supports num_experts <= %d and top_k <= %d", fn,
                     MAX_EXPERTS, MAX_TOPK);
     if (s.hidden % block_elems(s.gate_qtype) || s.expert_dim % block_elems(s.down_qtype))
-        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: hidden/expert_dim not whole blocks");
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: hidden/expert_dim not whole blocks", fn);
     if (s.hidden % 256 || s.expert_dim % 256)
-        return fail(QMOE_ERR_UNSUPPORTED, "moe_ffn: hidden and expert_dim must be multiples of 256");
+        return fail(QMOE_ERR_UNSUPPORTED, "%s: hidden and expert_dim must be multiples of 256", fn);
     if (s.hidden > MAX_K || static_cast<int64_t>(s.top_k) * s.expert_dim > MAX_K)
-        return fail(QMOE_ERR_UNSUPPORTED, "moe_ffn: hidden or top_k*expert_dim exceeds %lld",
+        return fail(QMOE_ERR_UNSUPPORTED, "%s: hidden or top_k*expert_dim exceeds %lld", fn,
                     (long long)MAX_K);
-    if (ws_bytes < moe_ffn_workspace_size(&s))
-        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn: workspace %zu < %zu bytes", ws_bytes,
-                    moe_ffn_workspace_size(&s));
+    if (ws_bytes < need)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: workspace %zu < %zu bytes", fn, ws_bytes,
+                    need);
     if (!aligned(router_W, 16) || !aligned(gate_stack, 16) || !aligned(up_stack, 16) ||
-        !aligned(down_stack, 16) || !aligned(x, 16) || !aligned(residual, 4) || !aligned(ws, 16))
+        !aligned(down_stack, 16) || !aligned(x, 16) || !aligned(residual, res_align) ||
+        !aligned(ws, 16))
         return fail(QMOE_ERR_INVALID_ARGUMENT,
-                    "moe_ffn: router, stacks, x and ws must be 16-byte aligned");
-    DevInfo* d = nullptr;
-    if (qmoe_status st = device_info(&d)) return st;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+                    "%s: router, stacks, x/norm weight and ws must be 16-byte aligned", fn);
+    return QMOE_OK;
+}
 
+// One MoE layer for s.n_tokens tokens.  With norm_w the input of token t is
+// ffn_norm(residual_t) and x is unused; xn is workspace for the normed
+// inputs of the tensor-core and separate-kernel forms.
+static qmoe_status moe_core(const float* router_W, const void* gate_stack, const void* up_stack,
+                            const void* down_stack, const qmoe_moe_shape& s, const float* x,
+                            const float* norm_w, float eps, float* residual, int32_t* topk_idx,
+                            float* topk_w, void* ws, float* xn, const DevInfo& dv,
+                            cudaStream_t st) {
+    const DevInfo* d = &dv;
+    if (prefill_path(&s) && norm_w) {
+        if (qmoe_status r = run_rmsnorm(residual, norm_w, s.n_tokens, s.hidden, eps, xn, st))
+            return r;
+        x = xn;
+    }
     if (prefill_path(&s))
         return run_prefill(router_W, gate_stack, up_stack, down_stack, s, x, residual, topk_idx,
                            topk_w, ws, *d, st);
@@ -797,7 +898,8 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
     const int64_t drb = row_bytes_of(s.down_qtype, F);
 
     for (int t = 0; t < s.n_tokens; ++t) {
-        const float* xt = x + static_cast<int64_t>(t) * H;
+        const float* xt = norm_w ? residual + static_cast<int64_t>(t) * H
+                                 : x + static_cast<int64_t>(t) * H;
         float* rt = residual + static_cast<int64_t>(t) * H;
         float* lt = logits + static_cast<int64_t>(t) * E;
 
@@ -848,16 +950,63 @@ qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* u
         f.topk = K;
         f.topk_idx_out = pg.topk_idx_out;
         f.topk_w_out = pg.topk_w_out;
+        f.norm_w = norm_w;
+        f.eps = eps;
         qmoe_status ferr = QMOE_OK;
         const int fr = dispatch_fused(s.gate_qtype, s.down_qtype, f, *d, st, &ferr);
         if (fr < 0) return ferr;
         if (fr > 0) continue;
         // the layer does not fit the fused kernel: router, gate/up, down
+        if (norm_w) {
+            float* xnt = xn + static_cast<int64_t>(t) * H;
+            if (qmoe_status r = run_rmsnorm(xt, norm_w, 1, H, eps, xnt, st)) return r;
+            xt = xnt;
+            pg.x = xt;
+        }
         if (qmoe_status r = run_f32_gemv(router_W, xt, lt, E, H, st)) return r;
         if (qmoe_status r = dispatch<MODE_GATEUP>(s.gate_qtype, pg, *d, st)) return r;
         if (qmoe_status r = dispatch<MODE_DOWN>(s.down_qtype, pd, *d, st)) return r;
     }
     return QMOE_OK;
+}
+
+qmoe_status moe_ffn(const float* router_W, const void* gate_stack, const void* up_stack,
+                    const void* down_stack, const qmoe_moe_shape* shape, const float* x,
+                    float* residual, int32_t* topk_idx, float* topk_w, void* ws,
+                    size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (qmoe_status r = moe_check("moe_ffn", router_W, gate_stack, up_stack, down_stack, shape, x,
+                                  residual, ws, ws_bytes, moe_ffn_workspace_size(shape), 4))
+        return r;
+    DevInfo* d = nullptr;
+    if (qmoe_status r = device_info(&d)) return r;
+    return moe_core(router_W, gate_stack, up_stack, down_stack, *shape, x, nullptr, 0.f, residual,
+                    topk_idx, topk_w, ws, nullptr, *d, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_ffn_rmsnorm_workspace_size(const qmoe_moe_shape* shape) {
+    const size_t base = moe_ffn_workspace_size(shape);
+    if (!base) return 0;
+    return base + static_cast<size_t>(shape->n_tokens) * static_cast<size_t>(shape->hidden) * 4;
+}
+
+qmoe_status moe_ffn_rmsnorm(const float* router_W, const void* gate_stack, const void* up_stack,
+                            const void* down_stack, const qmoe_moe_shape* shape,
+                            const float* norm_w, float eps, float* residual, int32_t* topk_idx,
+                            float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (qmoe_status r = moe_check("moe_ffn_rmsnorm", router_W, gate_stack, up_stack, down_stack,
+                                  shape, norm_w, residual, ws, ws_bytes,
+                                  moe_ffn_rmsnorm_workspace_size(shape), 16))
+        return r;
+    if (!(eps >= 0.f) || !std::isfinite(eps))
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "moe_ffn_rmsnorm: eps=%g must be finite, >= 0",
+                    static_cast<double>(eps));
+    DevInfo* d = nullptr;
+    if (qmoe_status r = device_info(&d)) return r;
+    float* xn = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + moe_ffn_workspace_size(shape));
+    return moe_core(router_W, gate_stack, up_stack, down_stack, *shape, nullptr, norm_w, eps,
+                    residual, topk_idx, topk_w, ws, xn, *d, static_cast<cudaStream_t>(stream));
 }
 
 // ----------------------------------------------------- allocation-free call

@@ -165,15 +165,41 @@ __device__ inline void route_topk(const float* __restrict__ logits, int E, int k
     group_sync(bar, nthr);
 }
 
+// ffn_norm's scale 1 / sqrt(mean(h^2) + eps) over h[0..n), computed by
+// threads [0, nthr) of the CTA (named barrier `bar`; red: NCW floats of
+// shared scratch).  Every participating thread gets the value.
+__device__ inline float rms_inverse(const float* __restrict__ h, int n, float eps, float* red,
+                                    int tid, int nthr, int bar) {
+    const float4* h4 = reinterpret_cast<const float4*>(h);
+    float ss = 0.f;
+    for (int i = tid; i < n / 4; i += nthr) {
+        const float4 v = __ldcg(h4 + i);
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    group_sync(bar, nthr);
+    float tot = 0.f;
+    for (int k = 0; k < nthr / 32; ++k) tot += red[k];
+    group_sync(bar, nthr);  // red may be reused after this
+    return 1.0f / sqrtf(tot / static_cast<float>(n) + eps);
+}
+
 template <class Fmt>
 __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, float* xq,
-                                    float* xs, int tid, int nthreads) {
+                                    float* xs, int tid, int nthreads,
+                                    const float* __restrict__ nw = nullptr, float inv = 1.f) {
     // x' in the per-quarter interleaved order; xs = sum of x per 16 elements.
     // A thread takes 16-element chunks of x: it loads the chunk's four
     // aligned float4s (all loads in flight before any use, so the table
     // costs one L2 round trip), stores their sum to xs, and scatters each
     // float4 to its x' slot (the formats' element orders keep every slot
     // four consecutive elements), each element scaled by its own power of two.
+    // With nw, the table is of the normed input x_j * inv * nw_j (ffn_norm).
     constexpr int UNR = 4;
     const int n16 = ngroups * 16;
     const float4* x4 = reinterpret_cast<const float4*>(x);
@@ -186,6 +212,17 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
             if (c < n16) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[u][k] = __ldcg(x4 + 4 * c + k);
+                if (nw) {
+                    const float4* w4 = reinterpret_cast<const float4*>(nw);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 wv = __ldg(w4 + 4 * c + k);
+                        v[u][k].x *= inv * wv.x;
+                        v[u][k].y *= inv * wv.y;
+                        v[u][k].z *= inv * wv.z;
+                        v[u][k].w *= inv * wv.w;
+                    }
+                }
             }
         }
 #pragma unroll

@@ -70,6 +70,11 @@ def expert_stack(g: np.random.Generator, qt: int, n_experts: int, rows: int,
     return m.reshape(n_experts, rows, -1)
 
 
+def norm_weight(g: np.random.Generator, n: int) -> np.ndarray:
+    """An ffn_norm weight vector: 1 + N(0, 0.1^2) per element, f32."""
+    return (1.0 + 0.1 * g.standard_normal(n)).astype(np.float32)
+
+
 def normal(g: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
     return (g.standard_normal(size=shape) * std).astype(np.float32)
 

@@ -106,3 +106,35 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qm, "_libh", None)
     with pytest.raises(qm.QmoeError):
         qm.lib()
+
+
+def test_rmsnorm_workspace_sizes(lib):
+    s = qm.moe_shape(2048, 768, 128, 8, 3, qm.Q4_K, qm.Q4_K, qm.Q6_K)
+    assert qm.moe_ffn_rmsnorm_workspace_size(s) == qm.moe_ffn_workspace_size(s) + 3 * 2048 * 4
+    assert qm.ffn_swiglu_rmsnorm_workspace_size(4096, 14336) >= \
+        qm.ffn_swiglu_workspace_size(4096, 14336) + 4096 * 4
+    assert qm.moe_ffn_rmsnorm_workspace_size(qm.moe_shape(0, 0, 0, 0, 0, 0, 0, 0)) == 0
+
+
+def test_rmsnorm_refusals(lib):
+    s = qm.moe_shape(2048, 768, 128, 8, 1, qm.Q4_K, qm.Q4_K, qm.Q6_K)
+    big = 1 << 24
+
+    def moe(norm=FAKE, eps=1e-6, res=FAKE, ws_bytes=big):
+        return lib.moe_ffn_rmsnorm(FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), norm, eps, res, None,
+                                   None, FAKE, ws_bytes, None)
+    assert moe(norm=None) == qm.ERR_INVALID_ARGUMENT
+    assert moe(eps=-1.0) == qm.ERR_INVALID_ARGUMENT
+    assert moe(eps=float("nan")) == qm.ERR_INVALID_ARGUMENT
+    assert moe(eps=float("inf")) == qm.ERR_INVALID_ARGUMENT
+    assert moe(res=FAKE + 4) == qm.ERR_INVALID_ARGUMENT   # the norm reads the residual as float4
+    assert moe(ws_bytes=qm.moe_ffn_workspace_size(s)) == qm.ERR_INVALID_ARGUMENT  # no room for xn
+    assert "moe_ffn_rmsnorm" in qm.last_error()
+
+    def ffn(norm=FAKE, eps=1e-6, ws_bytes=big):
+        return lib.ffn_swiglu_rmsnorm(FAKE, FAKE, FAKE, qm.Q4_K, qm.Q4_K, qm.Q6_K, 4096, 14336,
+                                      norm, eps, FAKE, FAKE, ws_bytes, None)
+    assert ffn(norm=None) == qm.ERR_INVALID_ARGUMENT
+    assert ffn(eps=-0.5) == qm.ERR_INVALID_ARGUMENT
+    assert ffn(ws_bytes=qm.ffn_swiglu_workspace_size(4096, 14336)) == qm.ERR_INVALID_ARGUMENT
+    assert "ffn_swiglu_rmsnorm" in qm.last_error()

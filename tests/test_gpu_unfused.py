@@ -15,8 +15,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def test_separate_kernel_path_parity():
     env = dict(os.environ, QMOE_FUSED="0")
     cmd = [sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_gpu_parity.py"),
+           os.path.join(ROOT, "tests", "test_gpu_rmsnorm.py"),
            "-m", "gpu", "-q", "-x", "-p", "no:cacheprovider",
-           "-k", "ffn_small or ffn_dense or moe_small or moe_decode"]
+           "-k", "ffn_small or ffn_dense or moe_small or moe_decode or rmsnorm"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
