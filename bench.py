@@ -372,6 +372,39 @@ def bench_layers(qm, synth, dev, stream, args):
     gn.replay()
     usn = time_replays(torch, gn, reps) * 1e3 / (reps * n)
     out["moe_decode"]["us_per_token_with_ffn_norm"] = round(usn, 3)
+    # small batches: T tokens per call, each routed expert read once per call
+    xpool2 = torch.cat([xpool, xpool])
+    per_expert = 2 * shp["expert_dim"] * rb_g + shp["hidden"] * rb_d
+    batched = {}
+    for T in (2, 4, 8, 16):
+        sT = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"], T,
+                          shp["gate"], shp["up"], shp["down"])
+        wsT = torch.zeros(qm.moe_ffn_workspace_size(sT), dtype=torch.uint8, device=dev)
+        resT = torch.from_numpy(synth.normal(synth.rng(97), (T, shp["hidden"]))).to(dev)
+        idxT = torch.empty((T, shp["top_k"]), dtype=torch.int32, device=dev)
+
+        def bcall(i, T=T, sT=sT, wsT=wsT, resT=resT, idxT=idxT):
+            j = (i * T) % 64
+            qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], sT, xpool2[j:j + T], resT,
+                       idxT, None, wsT)
+        nT = max(8, 64 // T)
+        experts = []
+        for i in range(nT):  # distinct experts each call reads
+            bcall(i)
+            experts.append(len(np.unique(idxT.cpu().numpy())))
+        gb = capture(torch, bcall, nT)
+        gb.replay()
+        usb = time_replays(torch, gb, reps) * 1e3 / (reps * nT)
+        ne = float(np.mean(experts))
+        algb = shp["num_experts"] * shp["hidden"] * 4 + ne * per_expert + 3 * T * shp["hidden"] * 4
+        batched[str(T)] = {"us_per_call": round(usb, 3), "us_per_token": round(usb / T, 3),
+                           "experts_read": round(ne, 2), "gbs": round(algb / usb / 1e3, 1),
+                           "frac": round(algb / usb / 1e3 / peak, 3)}
+        del gb
+    out["moe_decode"]["batched"] = batched
+    out["moe_decode"]["batched_launch"] = ("CUDA graph of max(8, 64/T) calls of T tokens; "
+                                           "alg bytes = router + distinct experts read + x, "
+                                           "residual in/out")
     del d, inp, gm, gn
     torch.cuda.empty_cache()
 
@@ -505,8 +538,8 @@ def run_reference(args, rank, world):
 
 def run_profile_case(case, launches):
     """Minimal program for ncu: one workload, `launches` calls, nothing else.
-    gemv:<FMT>[:rows] — one [rows]x4096 GEMV (default 4096 rows); moe — the decode layer;
-    ffn — the dense FFN."""
+    gemv:<FMT>[:rows] — one [rows]x4096 GEMV (default 4096 rows); moe[:T] — the decode layer
+    for T tokens (default 1); ffn — the dense FFN."""
     import torch
 
     import moe_ffn_gb300 as qm
@@ -524,10 +557,11 @@ def run_profile_case(case, launches):
         y = torch.empty(rows, device=dev)
         for _ in range(launches):
             qm.qmv(qt, W, rows, COLS, x, y)
-    elif case == "moe":
-        shp = synth.MOE_DECODE
+    elif case == "moe" or case.startswith("moe:"):
+        T = int(case.split(":")[1]) if ":" in case else 1
+        shp = dict(synth.MOE_DECODE, n_tokens=T)
         inp = synth.moe_inputs(0, **shp)
-        s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"], 1,
+        s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"], T,
                          shp["gate"], shp["up"], shp["down"])
         d = {k: torch.from_numpy(inp[k]).to(dev) for k in inp}
         ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device=dev)

@@ -32,7 +32,9 @@ OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-ftz=false",
-              "-std=c++17", "-Xcompiler", "-fPIC", "-shared"]
+              "-std=c++17", "-Xcompiler", "-fPIC"]
+# Translation units of libqmoe.so, compiled in parallel and linked together.
+UNITS = ("qmoe.cu", "batch.cu")
 
 
 class QmoeError(RuntimeError):
@@ -55,12 +57,29 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = os.environ.get("NVCC", "nvcc")
     if not os.path.exists(nvcc) and os.path.exists("/usr/local/cuda/bin/nvcc"):
         nvcc = "/usr/local/cuda/bin/nvcc"
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = [nvcc, *NVCC_FLAGS, "-o", tmp, os.path.join(_CSRC, "qmoe.cu")]
-    if verbose:
-        print(" ".join(cmd))
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    tag = f".{os.getpid()}.tmp"
+    objs = [os.path.join(_HERE, u.replace(".cu", f".{os.getpid()}.o")) for u in UNITS]
+    procs = []
+    for u, o in zip(UNITS, objs):
+        cmd = [nvcc, *NVCC_FLAGS, "-c", "-o", o, os.path.join(_CSRC, u)]
+        if verbose:
+            print(" ".join(cmd))
+        procs.append(subprocess.Popen(cmd))
+    codes = [p.wait() for p in procs]
+    try:
+        for u, c in zip(UNITS, codes):
+            if c:
+                raise subprocess.CalledProcessError(c, f"nvcc {u}")
+        tmp = LIB_PATH + tag
+        cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp, *objs]
+        if verbose:
+            print(" ".join(cmd))
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB_PATH
 
 

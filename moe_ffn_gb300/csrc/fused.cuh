@@ -150,11 +150,6 @@ __device__ __forceinline__ void sync_close(unsigned long long* sync) {
     }
 }
 
-// Prefetch `bytes` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 template <class FmtG, class FmtD>
 __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f) {
     extern __shared__ __align__(128) uint8_t smem[];

@@ -17,6 +17,7 @@
 #include "ptx.cuh"
 #include "stream.cuh"
 #include "fused.cuh"
+#include "batch.cuh"
 #include "prefill.cuh"
 
 namespace qmoe {
@@ -144,66 +145,6 @@ static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cud
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
-// Chunk geometry of a streamed phase for a stage budget (bytes): how rows
-// are cut into chunks, the slot strides and the bytes one stage needs.
-// False if not even one group per row fits.
-template <class Fmt, int MODE>
-static bool plan_chunks(StreamParams& p, int budget) {
-    using G = ModeGeom<MODE>;
-    if (budget < G::ROWS * (Fmt::SBB + 31)) return false;
-    const int seg_full = p.nb_seg * Fmt::SBB;
-    // Whole k-segments fit: runs of consecutive rows, one bulk copy each.
-    // A k-segment region holds the tile's rows at their global stride plus
-    // slack for up to four run starts (32 bytes apart), a 16-byte phase and
-    // the 14 bytes a Q6_K lane may read past its super-block.
-    // Rows of 2 KB and more stream at the full rate as separate copies, so
-    // formats whose loads would conflict at the global stride keep padded
-    // per-row slots for them.
-    const int run_piece = align_up(G::ROWS * seg_full, 16) + 144;
-    if (run_piece <= budget && (Fmt::RUNS_OK || seg_full < 2048)) {
-        p.runs = 1;
-        p.n_sbc = 1;
-        p.chunk_ks = budget / run_piece < p.n_kseg ? budget / run_piece : p.n_kseg;
-        p.chunk_sb = p.nb_seg;
-        p.piece_stride = run_piece;
-        p.slot_stride = seg_full;
-        p.stage_bytes = p.chunk_ks * run_piece;
-        p.n_chunk = (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks;
-        return true;
-    }
-    p.runs = 0;
-    const int piece_full = align_up(seg_full + 15, 16);
-    int nbp_max;
-    if (G::ROWS * p.n_kseg * piece_full <= budget) {
-        p.n_sbc = 1;
-        p.chunk_ks = p.n_kseg;
-        p.chunk_sb = p.nb_seg;
-        nbp_max = p.nb_seg;
-    } else if (G::ROWS * piece_full <= budget) {
-        p.n_sbc = 1;
-        p.chunk_ks = budget / (G::ROWS * piece_full);
-        p.chunk_sb = p.nb_seg;
-        nbp_max = p.nb_seg;
-    } else {
-        p.chunk_ks = 1;
-        int csb = (budget / G::ROWS - 31) / Fmt::SBB;
-        if (csb >= G::WK) csb -= csb % G::WK;
-        if (csb < 1) csb = 1;
-        p.chunk_sb = csb;
-        p.n_sbc = (p.nb_seg + csb - 1) / csb;
-        nbp_max = csb;
-    }
-    p.piece_stride = align_up(nbp_max * Fmt::SBB + 15, 16);
-    p.slot_stride = p.chunk_ks * p.piece_stride;
-    if (Fmt::SLOT_REM128 >= 0)
-        p.slot_stride += (Fmt::SLOT_REM128 - p.slot_stride % 128 + 128) % 128;
-    else if (p.slot_stride % 32 == 0)
-        p.slot_stride += 16;  // alternate rows across bank halves
-    p.stage_bytes = G::ROWS * p.slot_stride;
-    p.n_chunk = (p.n_sbc == 1) ? (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks : p.n_kseg * p.n_sbc;
-    return true;
 }
 
 // Plan chunking and pipeline depth for a streamed GEMV; false if it cannot
@@ -372,6 +313,16 @@ static bool fused_enabled() {
     static const bool on = [] {
         const char* e = getenv("QMOE_FUSED");
         return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+// The batched decode kernel for 2..31 tokens (QMOE_BATCH=0 runs those
+// tokens one fused launch at a time instead, for diagnostics).
+static bool batch_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("QMOE_BATCH");
+        return fused_enabled() && !(e && e[0] == '0');
     }();
     return on;
 }
@@ -710,8 +661,12 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* s) {
     if (!s || s->n_tokens <= 0 || s->num_experts <= 0 || s->top_k <= 0 || s->expert_dim <= 0 ||
         s->hidden <= 0)
         return 0;
-    const size_t decode = WS_SYNC_BYTES + moe_logits_bytes(s) +
-                          static_cast<size_t>(align_up(s->top_k * s->expert_dim * 4, 256));
+    // activations of one token, or of the (token, expert) pairs of one
+    // batched launch
+    const int tb = s->n_tokens < TB_MAX ? s->n_tokens : TB_MAX;
+    const size_t decode =
+        WS_SYNC_BYTES + moe_logits_bytes(s) +
+        static_cast<size_t>(align_up(tb * s->top_k * s->expert_dim * 4, 256));
     if (prefill_path(s)) {
         const size_t pf = pf_ws_layout(s).total;
         return pf > decode ? pf : decode;
@@ -896,6 +851,61 @@ static qmoe_status moe_core(const float* router_W, const void* gate_stack, const
                                         moe_logits_bytes(&s));
     const int64_t grb = row_bytes_of(s.gate_qtype, H), urb = row_bytes_of(s.up_qtype, H);
     const int64_t drb = row_bytes_of(s.down_qtype, F);
+
+    // Several tokens: batched launches that read each routed expert once for
+    // all the tokens routed to it, the tokens split evenly over the launches.
+    if (s.n_tokens >= 2 && batch_enabled()) {
+        const int tmax = batch_tokens_max(s.gate_qtype, s.down_qtype, H, F, K, d->smem_optin);
+        if (tmax >= 2) {
+            const int nl = (s.n_tokens + tmax - 1) / tmax;
+            int t0 = 0;
+            for (int l = 0; l < nl; ++l) {
+                const int tn = (s.n_tokens - t0) / (nl - l);
+                BatchParams b = {};
+                b.gu.W0 = static_cast<const uint8_t*>(gate_stack);
+                b.gu.rb0 = grb;
+                b.gu.es0 = grb * F;
+                b.gu.W1 = static_cast<const uint8_t*>(up_stack);
+                b.gu.rb1 = urb;
+                b.gu.es1 = urb * F;
+                b.gu.F = F;
+                b.gu.E = E;
+                b.gu.topk = K;
+                b.gu.moe = 1;
+                b.dn.W0 = static_cast<const uint8_t*>(down_stack);
+                b.dn.rb0 = drb;
+                b.dn.es0 = drb * H;
+                b.dn.F = F;
+                b.dn.E = E;
+                b.dn.topk = K;
+                b.dn.moe = 1;
+                b.router = router_W;
+                b.x = (norm_w ? residual : x) + static_cast<int64_t>(t0) * H;
+                b.residual = residual + static_cast<int64_t>(t0) * H;
+                b.logits = logits + static_cast<int64_t>(t0) * E;
+                b.act = a;
+                b.sync = static_cast<unsigned long long*>(ws);
+                b.T = tn;
+                b.E = E;
+                b.H = H;
+                b.F = F;
+                b.topk = K;
+                b.topk_idx_out = topk_idx ? topk_idx + static_cast<int64_t>(t0) * K : nullptr;
+                b.topk_w_out = topk_w ? topk_w + static_cast<int64_t>(t0) * K : nullptr;
+                b.norm_w = norm_w;
+                b.eps = eps;
+                b.err = d->err;
+                cudaError_t ce = cudaSuccess;
+                const int r = run_batch(s.gate_qtype, s.down_qtype, b, d->sms, d->smem_optin,
+                                        &g_coop_pdl, st, &ce);
+                if (r < 0) return cuda_fail(ce, "batched MoE launch");
+                if (r == 0)
+                    return fail(QMOE_ERR_UNSUPPORTED, "batched MoE kernel refused %d tokens", tn);
+                t0 += tn;
+            }
+            return QMOE_OK;
+        }
+    }
 
     for (int t = 0; t < s.n_tokens; ++t) {
         const float* xt = norm_w ? residual + static_cast<int64_t>(t) * H

@@ -189,10 +189,11 @@ __device__ inline float rms_inverse(const float* __restrict__ h, int n, float ep
     return 1.0f / sqrtf(tot / static_cast<float>(n) + eps);
 }
 
-template <class Fmt>
+template <class Fmt, int UNR = 4>
 __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, float* xq,
                                     float* xs, int tid, int nthreads,
-                                    const float* __restrict__ nw = nullptr, float inv = 1.f) {
+                                    const float* __restrict__ nw = nullptr, float inv = 1.f,
+                                    const float* inv_tok = nullptr, int tok_n16 = 0) {
     // x' in the per-quarter interleaved order; xs = sum of x per 16 elements.
     // A thread takes 16-element chunks of x: it loads the chunk's four
     // aligned float4s (all loads in flight before any use, so the table
@@ -200,7 +201,9 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
     // float4 to its x' slot (the formats' element orders keep every slot
     // four consecutive elements), each element scaled by its own power of two.
     // With nw, the table is of the normed input x_j * inv * nw_j (ffn_norm).
-    constexpr int UNR = 4;
+    // With inv_tok, x holds several tokens of tok_n16 chunks each, token t
+    // normed with inv_tok[t] (nw applies per token).  UNR chunks per thread
+    // are in flight at once.
     const int n16 = ngroups * 16;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     float4* xq4 = reinterpret_cast<float4*>(xq);
@@ -213,14 +216,21 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[u][k] = __ldcg(x4 + 4 * c + k);
                 if (nw) {
+                    int cw = c;
+                    float iv = inv;
+                    if (inv_tok) {
+                        const int tk = c / tok_n16;
+                        cw = c - tk * tok_n16;
+                        iv = inv_tok[tk];
+                    }
                     const float4* w4 = reinterpret_cast<const float4*>(nw);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float4 wv = __ldg(w4 + 4 * c + k);
-                        v[u][k].x *= inv * wv.x;
-                        v[u][k].y *= inv * wv.y;
-                        v[u][k].z *= inv * wv.z;
-                        v[u][k].w *= inv * wv.w;
+                        const float4 wv = __ldg(w4 + 4 * cw + k);
+                        v[u][k].x *= iv * wv.x;
+                        v[u][k].y *= iv * wv.y;
+                        v[u][k].z *= iv * wv.z;
+                        v[u][k].w *= iv * wv.w;
                     }
                 }
             }
@@ -349,6 +359,11 @@ __device__ __forceinline__ int run_dst(const StreamParams& p, int head, int idx)
     return ((head * p.slot_stride + 15) & ~15) + 32 * idx;
 }
 
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // The stage ring: nstages stages of stage_bytes, a full barrier (one
 // arrival + transaction bytes) and an empty barrier (NCW consumer warps)
 // per stage.  Producer and consumers number chunks with one running count
@@ -366,6 +381,56 @@ __device__ __forceinline__ int tile_slot(const StreamParams& p, int64_t u0) {
     return (MODE == MODE_GATEUP && p.moe) ? static_cast<int>(static_cast<uint32_t>(u0) /
                                                              static_cast<uint32_t>(p.F))
                                           : 0;
+}
+
+// The bulk copies of one chunk: runs, one copy per run of consecutive rows
+// and k-segment (gate/up tiles: 4 runs); otherwise one copy per row and
+// k-segment.  chunk_copies counts them, chunk_copy gives copy k (source,
+// bytes, stage offset; 0 bytes if the copy is empty).
+template <int MODE>
+__device__ __forceinline__ int chunk_copies(const StreamParams& p, const ChunkDesc& cd) {
+    using G = ModeGeom<MODE>;
+    constexpr int NR = (MODE == MODE_GATEUP) ? 4 : 1;
+    return p.runs ? NR * cd.nks : G::ROWS * cd.nks;
+}
+
+template <class Fmt, int MODE>
+__device__ __forceinline__ uint32_t chunk_copy(const StreamParams& p, const int32_t* s_idx,
+                                               int64_t u0, int s0, int64_t uend,
+                                               const ChunkDesc& cd, int k, uintptr_t& src,
+                                               int& dst) {
+    using G = ModeGeom<MODE>;
+    if (p.runs) {
+        constexpr int NR = (MODE == MODE_GATEUP) ? 4 : 1;
+        const int pk = k / NR, ri = k % NR;
+        const int nrow = static_cast<int>(uend - u0 < G::TU ? uend - u0 : G::TU);
+        int h = 0, e = nrow;  // rows [h, e) of this run
+        if (MODE == MODE_GATEUP) {
+            int jb = 16;
+            if (p.moe) {
+                const int64_t b = static_cast<int64_t>(s0 + 1) * p.F - u0;
+                jb = b < 16 ? static_cast<int>(b) : 16;
+            }
+            const int lo = (ri & 1) ? jb : 0, hi = (ri & 1) ? 16 : jb;
+            h = (ri >> 1) * 16 + lo;
+            e = (ri >> 1) * 16 + (hi < nrow ? hi : nrow);
+        }
+        if (e <= h) return 0u;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(
+            row_addr<MODE>(p, s_idx, u0, s0, uend, h, cd.ks0 + pk));
+        src = a & ~uintptr_t(15);
+        dst = pk * p.piece_stride + run_dst(p, h, ri);
+        return static_cast<uint32_t>(
+            ((a + static_cast<uintptr_t>(e - h) * p.slot_stride + 15) & ~uintptr_t(15)) - src);
+    }
+    const int r = k / cd.nks, pk = k % cd.nks;
+    const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, r, cd.ks0 + pk);
+    if (!a) return 0u;
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(a) + static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
+    src = sa & ~uintptr_t(15);
+    dst = r * p.slot_stride + pk * p.piece_stride;
+    return static_cast<uint32_t>(
+        ((sa + static_cast<uintptr_t>(cd.nbp) * Fmt::SBB + 15) & ~uintptr_t(15)) - src);
 }
 
 // Producer warp: stream every chunk of the units [ubeg, uend) into the ring.
@@ -386,60 +451,12 @@ __device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int
                 !mbar_wait_bounded(&ring.empty[s], (round - 1) & 1, p.err, DEV_TIMEOUT_EMPTY))
                 return false;
             const ChunkDesc cd = chunk_desc(p, c);
-            if (p.runs) {
-                // copy k: k-segment k / NR, run k % NR (gate/up: 4 runs)
-                constexpr int NR = (MODE == MODE_GATEUP) ? 4 : 1;
-                const int ncopy = NR * cd.nks;
-                const int nrow = static_cast<int>(uend - u0 < G::TU ? uend - u0 : G::TU);
-                uint32_t mine = 0;
-                uintptr_t csrc = 0;
-                uint32_t cbytes = 0;
-                int cdst = 0;
-                if (lane < ncopy) {  // at most 4 * MAX_TOPK / 2 copies: one per lane
-                    const int pk = lane / NR, ri = lane % NR;
-                    int h = 0, e = nrow;  // rows [h, e) of this run
-                    if (MODE == MODE_GATEUP) {
-                        int jb = 16;
-                        if (p.moe) {
-                            const int64_t b = static_cast<int64_t>(s0 + 1) * p.F - u0;
-                            jb = b < 16 ? static_cast<int>(b) : 16;
-                        }
-                        const int lo = (ri & 1) ? jb : 0, hi = (ri & 1) ? 16 : jb;
-                        h = (ri >> 1) * 16 + lo;
-                        e = (ri >> 1) * 16 + (hi < nrow ? hi : nrow);
-                    }
-                    if (e > h) {
-                        const uintptr_t src = reinterpret_cast<uintptr_t>(
-                            row_addr<MODE>(p, s_idx, u0, s0, uend, h, cd.ks0 + pk));
-                        csrc = src & ~uintptr_t(15);
-                        cbytes = static_cast<uint32_t>(
-                            ((src + static_cast<uintptr_t>(e - h) * p.slot_stride + 15) &
-                             ~uintptr_t(15)) - csrc);
-                        cdst = pk * p.piece_stride + run_dst(p, h, ri);
-                        mine = cbytes;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-                if (lane == 0) mbar_arrive_expect_tx(&ring.full[s], mine);
-                __syncwarp();
-                if (cbytes)
-                    bulk_g2s(ring.stages + static_cast<size_t>(s) * ring.stage_bytes + cdst,
-                             reinterpret_cast<const void*>(csrc), cbytes, &ring.full[s], pol);
-                continue;
-            }
-            const int ncopy = G::ROWS * cd.nks;
-            const uint32_t seg_bytes = static_cast<uint32_t>(cd.nbp * Fmt::SBB);
+            const int ncopy = chunk_copies<MODE>(p, cd);
             uint32_t mine = 0;
             for (int k = lane; k < ncopy; k += 32) {
-                const int r = k / cd.nks, pk = k % cd.nks;
-                const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, r, cd.ks0 + pk);
-                if (a) {
-                    const uintptr_t src = reinterpret_cast<uintptr_t>(a) +
-                                          static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
-                    const uintptr_t lo = src & ~uintptr_t(15);
-                    mine += static_cast<uint32_t>(((src + seg_bytes + 15) & ~uintptr_t(15)) - lo);
-                }
+                uintptr_t src = 0;
+                int dst = 0;
+                mine += chunk_copy<Fmt, MODE>(p, s_idx, u0, s0, uend, cd, k, src, dst);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
@@ -447,22 +464,17 @@ __device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int
             __syncwarp();
             uint8_t* st = ring.stages + static_cast<size_t>(s) * ring.stage_bytes;
             for (int k = lane; k < ncopy; k += 32) {
-                const int r = k / cd.nks, pk = k % cd.nks;
-                const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, r, cd.ks0 + pk);
-                if (a) {
-                    const uintptr_t src = reinterpret_cast<uintptr_t>(a) +
-                                          static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
-                    const uintptr_t lo = src & ~uintptr_t(15);
-                    const uint32_t n =
-                        static_cast<uint32_t>(((src + seg_bytes + 15) & ~uintptr_t(15)) - lo);
-                    bulk_g2s(st + r * p.slot_stride + pk * p.piece_stride,
-                             reinterpret_cast<const void*>(lo), n, &ring.full[s], pol);
-                }
+                uintptr_t src = 0;
+                int dst = 0;
+                const uint32_t n = chunk_copy<Fmt, MODE>(p, s_idx, u0, s0, uend, cd, k, src, dst);
+                if (n)
+                    bulk_g2s(st + dst, reinterpret_cast<const void*>(src), n, &ring.full[s], pol);
             }
         }
     }
     return true;
 }
+
 // Consumer warps 0..NCW-1: reduce every tile of [ubeg, uend) and write the
 // outputs (QMV: y = W.x; GATEUP: a = w * silu(g) * u; DOWN: out += D.a).
 // x' / xs must already hold the phase's input.  False (in every consumer
@@ -662,6 +674,67 @@ __global__ void __launch_bounds__(NTHREADS) stream_gemv_kernel(const StreamParam
     named_bar(1, NCW * 32);
     if (!p.moe) named_bar(2, NTHREADS);  // the stage barriers are initialised
     consume_phase<Fmt, MODE>(p, ring, s_idx, s_w, xq, xs, part, ubeg, uend, it, tid);
+}
+
+// ------------------------------------------------------------ host planning
+// Chunk geometry of a streamed phase for a stage budget (bytes): how rows
+// are cut into chunks, the slot strides and the bytes one stage needs.
+// False if not even one group per row fits.
+template <class Fmt, int MODE>
+inline bool plan_chunks(StreamParams& p, int budget) {
+    using G = ModeGeom<MODE>;
+    if (budget < G::ROWS * (Fmt::SBB + 31)) return false;
+    const int seg_full = p.nb_seg * Fmt::SBB;
+    // Whole k-segments fit: runs of consecutive rows, one bulk copy each.
+    // A k-segment region holds the tile's rows at their global stride plus
+    // slack for up to four run starts (32 bytes apart), a 16-byte phase and
+    // the 14 bytes a Q6_K lane may read past its super-block.
+    // Rows of 2 KB and more stream at the full rate as separate copies, so
+    // formats whose loads would conflict at the global stride keep padded
+    // per-row slots for them.
+    const int run_piece = align_up(G::ROWS * seg_full, 16) + 144;
+    if (run_piece <= budget && (Fmt::RUNS_OK || seg_full < 2048)) {
+        p.runs = 1;
+        p.n_sbc = 1;
+        p.chunk_ks = budget / run_piece < p.n_kseg ? budget / run_piece : p.n_kseg;
+        p.chunk_sb = p.nb_seg;
+        p.piece_stride = run_piece;
+        p.slot_stride = seg_full;
+        p.stage_bytes = p.chunk_ks * run_piece;
+        p.n_chunk = (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks;
+        return true;
+    }
+    p.runs = 0;
+    const int piece_full = align_up(seg_full + 15, 16);
+    int nbp_max;
+    if (G::ROWS * p.n_kseg * piece_full <= budget) {
+        p.n_sbc = 1;
+        p.chunk_ks = p.n_kseg;
+        p.chunk_sb = p.nb_seg;
+        nbp_max = p.nb_seg;
+    } else if (G::ROWS * piece_full <= budget) {
+        p.n_sbc = 1;
+        p.chunk_ks = budget / (G::ROWS * piece_full);
+        p.chunk_sb = p.nb_seg;
+        nbp_max = p.nb_seg;
+    } else {
+        p.chunk_ks = 1;
+        int csb = (budget / G::ROWS - 31) / Fmt::SBB;
+        if (csb >= G::WK) csb -= csb % G::WK;
+        if (csb < 1) csb = 1;
+        p.chunk_sb = csb;
+        p.n_sbc = (p.nb_seg + csb - 1) / csb;
+        nbp_max = csb;
+    }
+    p.piece_stride = align_up(nbp_max * Fmt::SBB + 15, 16);
+    p.slot_stride = p.chunk_ks * p.piece_stride;
+    if (Fmt::SLOT_REM128 >= 0)
+        p.slot_stride += (Fmt::SLOT_REM128 - p.slot_stride % 128 + 128) % 128;
+    else if (p.slot_stride % 32 == 0)
+        p.slot_stride += 16;  // alternate rows across bank halves
+    p.stage_bytes = G::ROWS * p.slot_stride;
+    p.n_chunk = (p.n_sbc == 1) ? (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks : p.n_kseg * p.n_sbc;
+    return true;
 }
 
 }  // namespace qmoe

@@ -42,6 +42,7 @@ def test_ffn_swiglu_rmsnorm(qm, orc, H, F, gq, dq):
 MOE_NORM = [
     dict(hidden=2048, expert_dim=768, num_experts=128, top_k=8, n_tokens=1),   # decode shape
     dict(hidden=512, expert_dim=512, num_experts=16, top_k=4, n_tokens=3),     # a few tokens
+    dict(hidden=2048, expert_dim=768, num_experts=128, top_k=8, n_tokens=16),  # batched decode
     dict(hidden=256, expert_dim=256, num_experts=8, top_k=2, n_tokens=64),     # tensor cores
 ]
 

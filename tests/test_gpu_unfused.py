@@ -1,7 +1,11 @@
-"""The separate-kernel path of ffn_swiglu and moe_ffn (router GEMV, gate/up,
-down as three launches), which the library takes when a layer does not fit
-the fused kernel.  QMOE_FUSED=0 forces it; the switch is read once per
-process, so the parity tests run again in a child process with it set."""
+"""Paths the library takes only when the default one does not apply, run in
+child processes with the switch that forces them (each switch is read once
+per process):
+  - QMOE_FUSED=0: the separate-kernel form of ffn_swiglu and moe_ffn (router
+    GEMV, gate/up, down as three launches), taken when a layer does not fit
+    the fused kernel;
+  - QMOE_BATCH=0: 2..31 tokens as one fused launch per token, taken when the
+    batched kernel's tiles do not fit shared memory."""
 import os
 import subprocess
 import sys
@@ -18,6 +22,18 @@ def test_separate_kernel_path_parity():
            os.path.join(ROOT, "tests", "test_gpu_rmsnorm.py"),
            "-m", "gpu", "-q", "-x", "-p", "no:cacheprovider",
            "-k", "ffn_small or ffn_dense or moe_small or moe_decode or rmsnorm"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout
+
+
+@pytest.mark.gpu
+def test_token_by_token_path_parity():
+    env = dict(os.environ, QMOE_BATCH="0")
+    cmd = [sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_gpu_batch.py"),
+           os.path.join(ROOT, "tests", "test_gpu_rmsnorm.py"),
+           "-m", "gpu", "-q", "-x", "-p", "no:cacheprovider",
+           "-k", "all_tokens or moe_ffn_rmsnorm"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
