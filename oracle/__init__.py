@@ -71,7 +71,7 @@ def _load():
             lib.orc_matvec_fused.restype = ctypes.c_int
             lib.orc_matvec_fused.argtypes = [ctypes.c_int, P, i64, i64, P, P]
             lib.orc_route.restype = ctypes.c_int
-            lib.orc_route.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P]
+            lib.orc_route.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
             lib.orc_moe_ffn.restype = ctypes.c_int
             lib.orc_moe_ffn.argtypes = [P, i64, P, P, P, P, P, P, P, P, P, P, P, P, P]
             lib.orc_ffn_swiglu.restype = ctypes.c_int
@@ -151,13 +151,15 @@ def matvec_fused(qt: int, W, rows: int, cols: int, x) -> np.ndarray:
     return y
 
 
-def route(logits, k: int):
-    """(idx, w): the k routed experts in rank order and their renormalised weights."""
+def route(logits, k: int, renormalize: bool = True):
+    """(idx, w): the k routed experts in rank order and their weights,
+    renormalised over the k (default) or the softmax probabilities over all
+    experts (renormalize=False)."""
     lg = np.ascontiguousarray(logits, dtype=np.float64)
     E = lg.size
     idx = np.zeros(k, np.int32)
     w = np.zeros(k, np.float64)
-    rc = _load().orc_route(_ptr(lg), E, k, _ptr(idx), _ptr(w))
+    rc = _load().orc_route(_ptr(lg), E, k, int(bool(renormalize)), _ptr(idx), _ptr(w))
     if rc != 0:
         raise ValueError(f"orc_route rejected E={E} k={k}")
     return idx, w
@@ -167,13 +169,14 @@ class _Shape(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("expert_dim", ctypes.c_int32),
                 ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("gate_qt", ctypes.c_int32), ("up_qt", ctypes.c_int32),
-                ("down_qt", ctypes.c_int32)]
+                ("down_qt", ctypes.c_int32), ("no_renorm", ctypes.c_int32)]
 
 
 def moe_ffn(hidden, expert_dim, num_experts, top_k, gate_qt, up_qt, down_qt,
-            router, gate, up, down, x, residual, tokens=None):
+            router, gate, up, down, x, residual, tokens=None, renormalize=True):
     """MoE FFN per token.  x, residual: [T][hidden].  ``tokens`` (optional)
     restricts the computation to those token rows (sampled checks).
+    ``renormalize`` selects the routing weights (see route).
 
     Returns dict(out [T'][hidden] f64, tol, idx [T'][k], w [T'][k], gap [T'],
     logits [T'][E], lscale [T'] = max_e sum_j |R_ej x_j|)."""
@@ -184,7 +187,8 @@ def moe_ffn(hidden, expert_dim, num_experts, top_k, gate_qt, up_qt, down_qt,
         x = np.ascontiguousarray(x[tokens])
         residual = np.ascontiguousarray(residual[tokens])
     T = x.shape[0]
-    sh = _Shape(hidden, expert_dim, num_experts, top_k, gate_qt, up_qt, down_qt)
+    sh = _Shape(hidden, expert_dim, num_experts, top_k, gate_qt, up_qt, down_qt,
+                0 if renormalize else 1)
     router = np.ascontiguousarray(router, dtype=np.float32)
     out = np.zeros((T, hidden), np.float64)
     tol = np.zeros((T, hidden), np.float64)

@@ -309,8 +309,11 @@ int orc_matvec_fused(int qt, const uint8_t *W, int64_t rows, int64_t cols, const
  * Readings (the routing function's body is not on the pages): softmax in
  * double with the maximum subtracted; ranking by probability, descending,
  * equal probabilities ranked by the lower expert index; w_s = p_s / sum
- * of the k selected p. */
-int orc_route(const double *logits, int E, int k, int32_t *idx, double *w) {
+ * of the k selected p.
+ * renorm = 0 skips the last step (w_s = p_s, the softmax probability over
+ * all E experts): the pages do not say whether the OLMoE-shaped layer
+ * renormalises, so both readings are available. */
+int orc_route(const double *logits, int E, int k, int renorm, int32_t *idx, double *w) {
     if (E <= 0 || k <= 0 || k > E) return -1;
     double mx = logits[0];
     for (int e = 1; e < E; e++)
@@ -331,6 +334,7 @@ int orc_route(const double *logits, int E, int k, int32_t *idx, double *w) {
     }
     double s = 0.0;
     for (int i = 0; i < k; i++) s += p[order[i]];
+    if (!renorm) s = 1.0;
     for (int i = 0; i < k; i++) { idx[i] = order[i]; w[i] = p[order[i]] / s; }
     free(p);
     free(order);
@@ -373,7 +377,9 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
  *         + 2^-22 |out_i| + 1e-6
  *   da = |silu'(g) u| dg + |silu(g)| du,  dg_j = 1e-3 S^G_j + 1e-6 (du alike)
  *   dw_s = 2 w_s (1 - w_s) max_t dl_t,  dl_t = 1e-3 sum_j |R_tj x_j| + 1e-6
- *   (dw_s/dl_t = w_s (delta_st - w_t), so |dw_s| <= 2 w_s (1 - w_s) max |dl|).
+ *   (dw_s/dl_t = w_s (delta_st - w_t) over the k renormalised weights, or
+ *   over all E softmax probabilities without renormalisation; either way
+ *   |dw_s| <= 2 w_s (1 - w_s) max |dl|).
  * route_idx/route_w (nullable) receive [T][k]; logit_gap (nullable)
  * receives per token the smallest gap among the top k+1 sorted logits
  * divided by max_t sum_j |R_tj x_j| (the ambiguity measure for ties);
@@ -382,6 +388,7 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 typedef struct {
     int32_t hidden, expert_dim, num_experts, top_k;
     int32_t gate_qt, up_qt, down_qt;
+    int32_t no_renorm;  /* 1: routing weights are not renormalised (orc_route) */
 } orc_moe_shape;
 
 static double dsilu(double g) {
@@ -431,7 +438,7 @@ int orc_moe_ffn(const orc_moe_shape *sh, int64_t T, const float *router, const u
             double d = 1e-3 * sa + 1e-6;
             if (d > dl) dl = d;
         }
-        orc_route(logits, E, K, idx, w);
+        orc_route(logits, E, K, !sh->no_renorm, idx, w);
         if (logits_out)
             for (int e = 0; e < E; e++) logits_out[t * E + e] = logits[e];
         if (lscale_out) {

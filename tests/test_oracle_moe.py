@@ -49,6 +49,30 @@ def test_moe_brute_force_numpy(orc):
         assert np.allclose(ref["out"][t], out, rtol=1e-10, atol=1e-9)
 
 
+def test_moe_without_renormalisation_brute_force(orc):
+    """renormalize=False: the same composition with w = the selected softmax
+    probabilities (no division by their sum)."""
+    shp = dict(SMALL, top_k=3)
+    inp = synth.moe_inputs(13, **shp)
+    H, F, E, K = shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"]
+    G = [orc.dequant(shp["gate"], inp["gate"][e], F, H).astype(np.float64) for e in range(E)]
+    U = [orc.dequant(shp["up"], inp["up"][e], F, H).astype(np.float64) for e in range(E)]
+    D = [orc.dequant(shp["down"], inp["down"][e], H, F).astype(np.float64) for e in range(E)]
+    ref = _run(orc, shp, inp, renormalize=False)
+    for t in range(shp["n_tokens"]):
+        x = inp["x"][t].astype(np.float64)
+        p = softmax(inp["router"].astype(np.float64) @ x)
+        sel = np.argsort(-p, kind="stable")[:K]
+        out = inp["residual"][t].astype(np.float64).copy()
+        for e in sel:
+            g, u = G[e] @ x, U[e] @ x
+            out += D[e] @ (p[e] * (g * expit(g) * u))
+        assert list(ref["idx"][t]) == list(sel)
+        assert np.allclose(ref["w"][t], p[sel], rtol=1e-12)
+        assert ref["w"][t].sum() < 1.0
+        assert np.allclose(ref["out"][t], out, rtol=1e-10, atol=1e-9)
+
+
 def test_one_expert_is_dense_ffn(orc):
     shp = dict(SMALL, num_experts=1, top_k=1, n_tokens=1)
     inp = synth.moe_inputs(12, **shp)

@@ -316,6 +316,35 @@ def test_route_brute_force_small(orc):
     assert sorted(idx) == sorted(best)
 
 
+def test_route_without_renormalisation_is_softmax_restricted(orc):
+    """renormalize=False: the same experts, weighted by their softmax
+    probability over all E experts (scipy), so the weights sum to the mass of
+    the top k; k = E sums to 1; two experts, top-1: the logistic function of
+    the logit difference."""
+    from scipy.special import expit, softmax
+    rng = np.random.default_rng(6)
+    for E, k in [(128, 8), (64, 8), (8, 1), (5, 3), (256, 16)]:
+        lg = rng.standard_normal(E) * 2
+        idx, w = orc.route(lg, k, renormalize=False)
+        idx_r, w_r = orc.route(lg, k)
+        p = softmax(lg)
+        order = np.argsort(-p, kind="stable")[:k]
+        assert list(idx) == list(order) == list(idx_r)
+        assert np.allclose(w, p[order], rtol=1e-13, atol=0)
+        assert abs(w.sum() - p[order].sum()) < 1e-13
+        assert w.sum() < 1.0 or k == E
+    lg = rng.standard_normal(12)
+    _, w = orc.route(lg, 12, renormalize=False)
+    assert abs(w.sum() - 1.0) < 1e-13
+    for a, b in [(0.3, -1.2), (2.0, 1.5), (-4.0, 3.0)]:
+        idx, w = orc.route(np.array([a, b]), 1, renormalize=False)
+        assert idx[0] == (0 if a >= b else 1)
+        assert abs(w[0] - expit(abs(a - b))) < 1e-15
+    # equal logits: 1/E each (1/k with renormalisation)
+    _, w = orc.route(np.zeros(10), 4, renormalize=False)
+    assert np.allclose(w, 0.1, rtol=1e-15)
+
+
 def test_route_rejects_bad_shape(orc):
     with pytest.raises(ValueError):
         orc.route(np.zeros(4), 5)
