@@ -88,7 +88,14 @@ typedef struct {
     int32_t gate_qtype;  /* qmoe_qtype of the gate stack (quantized) */
     int32_t up_qtype;    /* must equal gate_qtype */
     int32_t down_qtype;  /* qmoe_qtype of the down stack (quantized) */
+    int32_t route_flags; /* 0, or QMOE_ROUTE_NO_RENORM */
 } qmoe_moe_shape;
+
+/* route_flags: the routing weights are the softmax probabilities over all E
+ * experts of the k selected ones, not renormalised over the k.  The pages
+ * state renormalisation for the Qwen3-MoE-shaped layer and are silent for
+ * the OLMoE-shaped one; this flag gives the other reading. */
+#define QMOE_ROUTE_NO_RENORM 1
 
 /* y = W x — launch_q*_matvec on "ferrox-cuda 0.14.0 — src/gpu.rs" and
  * WeightMatrix::apply on "ferrox-core 0.16.0 — weight_matrix.rs".
@@ -163,7 +170,8 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
 /* The MoE FFN of one layer for T tokens — moe_layer on "aprender-serve
  * 0.70.2 — forward_qwen3_moe_resident.rs", after ffn_norm:
  *   logits = R x_t (F32 router [E][H]);  softmax over E, the top k (ties:
- *   lower expert index), weights renormalised over those k;
+ *   lower expert index), weights renormalised over those k (or, with
+ *   shape->route_flags = QMOE_ROUTE_NO_RENORM, the softmax probabilities);
  *   for each routed (e, w) in rank order:  a = silu(G_e x_t) * (U_e x_t),
  *   residual_t += D_e (w a).
  * The routing runs on the device: no host synchronisation inside the layer.
@@ -173,7 +181,7 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  *   down_stack  [E][H][F] quantized
  *   x           [T][H] f32 (normed input);  residual [T][H] f32, in place
  *   topk_idx    [T][k] int32 or NULL: routed experts in rank order
- *   topk_w      [T][k] f32 or NULL: their renormalised weights
+ *   topk_w      [T][k] f32 or NULL: their routing weights
  *   ws          >= moe_ffn_workspace_size(shape) bytes, 16-byte aligned;
  *               scratch that may hold anything before a call; calls that
  *               overlap on the GPU must not share one

@@ -87,7 +87,8 @@ class _Shape(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("expert_dim", ctypes.c_int32),
                 ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("n_tokens", ctypes.c_int32), ("gate_qtype", ctypes.c_int32),
-                ("up_qtype", ctypes.c_int32), ("down_qtype", ctypes.c_int32)]
+                ("up_qtype", ctypes.c_int32), ("down_qtype", ctypes.c_int32),
+                ("route_flags", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -184,10 +185,14 @@ def ffn_swiglu(gate, up, down, gate_qtype, up_qtype, down_qtype, hidden, inter, 
                             _stream(stream)))
 
 
+# shape.route_flags: routing weights are the softmax probabilities, not renormalised
+ROUTE_NO_RENORM = 1
+
+
 def moe_shape(hidden, expert_dim, num_experts, top_k, n_tokens, gate_qtype, up_qtype,
-              down_qtype) -> _Shape:
+              down_qtype, renormalize: bool = True) -> _Shape:
     return _Shape(hidden, expert_dim, num_experts, top_k, n_tokens, gate_qtype, up_qtype,
-                  down_qtype)
+                  down_qtype, 0 if renormalize else ROUTE_NO_RENORM)
 
 
 def moe_ffn_workspace_size(shape: _Shape) -> int:

@@ -105,11 +105,11 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 // Routing of one token by one warp: softmax over the E logits, the k
 // largest (ties: lower expert index), renormalised over those k — as
 // route_topk, with the same weights: w_s = exp(l_s - l_0) / sum over the k
-// selected.  Lane l holds experts [l*m, l*m + m), so among equal keys the
-// lowest lane holds the lowest index; k rounds of a warp max pick the ranks
-// in order.
+// selected (over all E with renorm = 0).  Lane l holds experts
+// [l*m, l*m + m), so among equal keys the lowest lane holds the lowest
+// index; k rounds of a warp max pick the ranks in order.
 __device__ __forceinline__ void route_warp(const float* __restrict__ lg, int E, int k, int lane,
-                                           int32_t* idx, float* w) {
+                                           int renorm, int32_t* idx, float* w) {
     constexpr int M = MAX_EXPERTS / 32;
     const int m = (E + 31) >> 5;
     uint32_t key[M];
@@ -151,6 +151,12 @@ __device__ __forceinline__ void route_warp(const float* __restrict__ lg, int E, 
     const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
     const float pr = lane < k ? expf(my_l - lmax) : 0.f;
     float z = pr;
+    if (!renorm) {
+        z = 0.f;
+#pragma unroll
+        for (int j = 0; j < M; ++j)
+            if (j < m && lane * m + j < E) z += expf(val[j] - lmax);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     if (lane < k) {
@@ -450,8 +456,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     }
     // routing: one warp per token
     for (int t = warp; t < T; t += NCW)
-        route_warp(b.logits + static_cast<int64_t>(t) * E, E, K, lane, s_ridx + t * K,
-                   s_rw + t * K);
+        route_warp(b.logits + static_cast<int64_t>(t) * E, E, K, lane, b.gu.renorm,
+                   s_ridx + t * K, s_rw + t * K);
     for (int e = tid; e < E; e += NC) s_mask[e] = 0u;
     named_bar(1, NC);
     if (cta == 0) {

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
             named_bar_arrive(2, NTHREADS);  // release the producer, which then returns
             return;
         }
-        route_topk(f.logits, f.E, f.topk, s_logit, s_idx, s_w, tid, NC, 1);
+        route_topk(f.logits, f.E, f.topk, s_logit, s_idx, s_w, tid, NC, 1, f.gu.renorm);
         if (cta == 0 && tid < f.topk) {
             if (f.topk_idx_out) f.topk_idx_out[tid] = s_idx[tid];
             if (f.topk_w_out) f.topk_w_out[tid] = s_w[tid];

@@ -6,7 +6,7 @@
 // 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 //   pf_router_kernel   logits[T][E] = X R^T in f32 (CUDA cores)
-//   pf_topk_kernel     per token: softmax/top-k/renormalise, the (token, slot)
+//   pf_topk_kernel     per token: softmax/top-k/renormalise (or not), the (token, slot)
 //                      pairs appended to each expert's list, x copied to f16
 //                      with a power-of-two scale
 //   pf_gateup_kernel   per (expert, 128 features): D_g = G X^T, D_u = U X^T
@@ -97,12 +97,12 @@ __global__ void __launch_bounds__(256) pf_router_kernel(const float* __restrict_
 
 // ------------------------------------------------------------------ top-k
 // One warp per token.  Routing as the decode path (softmax over E, the k
-// largest with ties to the lower index, renormalised); each (token, slot)
+// largest with ties to the lower index, renormalised unless renorm = 0); each (token, slot)
 // pair is appended to its expert's list.  x is copied to f16 scaled by
 // 2^s_t, s_t chosen so that max |x| * 2^s_t lies in [2^14, 2^15).
 __global__ void __launch_bounds__(256) pf_topk_kernel(
     const float* __restrict__ logits, const float* __restrict__ X, int T, int H, int E, int K,
-    int32_t* __restrict__ tidx, float* __restrict__ tw, int32_t* __restrict__ user_idx,
+    int renorm, int32_t* __restrict__ tidx, float* __restrict__ tw, int32_t* __restrict__ user_idx,
     float* __restrict__ user_w, int32_t* __restrict__ cnt, int32_t* __restrict__ list,
     __half* __restrict__ X16, float* __restrict__ xinv) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -147,6 +147,16 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(
         }
     }
     __syncwarp();
+    // without renormalisation the weights divide by the softmax sum over all E
+    float zall = 0.f;
+    if (!renorm) {
+        const float lmax = s_l[warp][0];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (lane + 32 * i < E) zall += expf(lv[i] - lmax);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) zall += __shfl_xor_sync(0xffffffffu, zall, o);
+    }
     if (lane == 0) {
         const float lmax = s_l[warp][0];
         float p[16], z = 0.f;
@@ -154,7 +164,7 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(
             p[s] = expf(s_l[warp][s] - lmax);
             z += p[s];
         }
-        const float inv = 1.0f / z;
+        const float inv = 1.0f / (renorm ? z : zall);
         for (int s = 0; s < K; ++s) {
             const int e = s_idx[warp][s];
             const float w = p[s] * inv;

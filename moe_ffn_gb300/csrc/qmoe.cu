@@ -733,9 +733,10 @@ static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
     cudaError_t e = launch_pdl(pf::pf_router_kernel, dim3((T + 7) / 8, (E + 31) / 32), dim3(256),
                                0, st, router_W, x, T, H, E, logits, cnt);
     if (e != cudaSuccess) return cuda_fail(e, "pf_router launch");
+    const int renorm = (s.route_flags & QMOE_ROUTE_NO_RENORM) ? 0 : 1;
     e = launch_pdl(pf::pf_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st,
-                   static_cast<const float*>(logits), x, T, H, E, K, tidx, tw, topk_idx, topk_w,
-                   cnt, list, x16, xinv);
+                   static_cast<const float*>(logits), x, T, H, E, K, renorm, tidx, tw, topk_idx,
+                   topk_w, cnt, list, x16, xinv);
     if (e != cudaSuccess) return cuda_fail(e, "pf_topk launch");
 
     static int configured[64] = {};
@@ -803,6 +804,9 @@ static qmoe_status moe_check(const char* fn, const float* router_W, const void* 
     if (s.top_k > s.num_experts)
         return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: top_k=%d > num_experts=%d", fn, s.top_k,
                     s.num_experts);
+    if (s.route_flags & ~QMOE_ROUTE_NO_RENORM)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "%s: unknown route_flags 0x%x", fn,
+                    static_cast<unsigned>(s.route_flags));
     if (qmoe_status st = check_ffn_qtypes(fn, s.gate_qtype, s.up_qtype, s.down_qtype))
         return st;
     if (s.num_experts > MAX_EXPERTS || s.top_k > MAX_TOPK)
@@ -846,6 +850,7 @@ static qmoe_status moe_core(const float* router_W, const void* gate_stack, const
                            topk_w, ws, *d, st);
 
     const int H = s.hidden, F = s.expert_dim, E = s.num_experts, K = s.top_k;
+    const int renorm = (s.route_flags & QMOE_ROUTE_NO_RENORM) ? 0 : 1;
     float* logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + WS_SYNC_BYTES);
     float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + WS_SYNC_BYTES +
                                         moe_logits_bytes(&s));
@@ -872,6 +877,7 @@ static qmoe_status moe_core(const float* router_W, const void* gate_stack, const
                 b.gu.E = E;
                 b.gu.topk = K;
                 b.gu.moe = 1;
+                b.gu.renorm = renorm;
                 b.dn.W0 = static_cast<const uint8_t*>(down_stack);
                 b.dn.rb0 = drb;
                 b.dn.es0 = drb * H;
@@ -879,6 +885,7 @@ static qmoe_status moe_core(const float* router_W, const void* gate_stack, const
                 b.dn.E = E;
                 b.dn.topk = K;
                 b.dn.moe = 1;
+                b.dn.renorm = renorm;
                 b.router = router_W;
                 b.x = (norm_w ? residual : x) + static_cast<int64_t>(t0) * H;
                 b.residual = residual + static_cast<int64_t>(t0) * H;
@@ -932,6 +939,7 @@ static qmoe_status moe_core(const float* router_W, const void* gate_stack, const
         pg.topk_idx_out = topk_idx ? topk_idx + static_cast<int64_t>(t) * K : nullptr;
         pg.topk_w_out = topk_w ? topk_w + static_cast<int64_t>(t) * K : nullptr;
         pg.moe = 1;
+        pg.renorm = renorm;
 
         StreamParams pd = {};
         pd.units = H;
@@ -947,6 +955,7 @@ static qmoe_status moe_core(const float* router_W, const void* gate_stack, const
         pd.topk = K;
         pd.F = F;
         pd.moe = 1;
+        pd.renorm = renorm;
 
         FusedParams f = {};
         f.gu = pg;

@@ -66,6 +66,7 @@ struct StreamParams {
     // routing (MoE): logits of this token, E experts, top-k, rows per expert
     const float* logits;
     int E, topk, F;
+    int renorm;             // 1: weights renormalised over the k; 0: softmax over all E
     int32_t* topk_idx_out;  // nullable, written by CTA 0 of GATEUP
     float* topk_w_out;
     int moe;
@@ -111,7 +112,9 @@ __host__ __device__ inline SmemLayout smem_layout(const StreamParams& p) {
 // renormalised over those k — the page's "softmax, top-k, renormalize" of
 // "aprender-serve 0.70.2 — forward_qwen3_moe_resident.rs" (module doc,
 // moe_layer).  The renormalised weight of a selected expert equals
-// exp(l_s - l_max) / sum over the selected k of exp(l_t - l_max).
+// exp(l_s - l_max) / sum over the selected k of exp(l_t - l_max); with
+// renorm = 0 the sum runs over all E experts instead (the softmax
+// probability itself).
 // Threads [0, nthr) of the CTA call it together; they synchronise on named
 // barrier `bar` (0: the whole CTA, nthr == blockDim.x).  k <= 32.
 __device__ __forceinline__ void group_sync(int bar, int nthr) {
@@ -122,7 +125,8 @@ __device__ __forceinline__ void group_sync(int bar, int nthr) {
 }
 
 __device__ inline void route_topk(const float* __restrict__ logits, int E, int k, float* s_logit,
-                                  int32_t* s_idx, float* s_w, int tid, int nthr, int bar) {
+                                  int32_t* s_idx, float* s_w, int tid, int nthr, int bar,
+                                  int renorm) {
     for (int e = tid; e < E; e += nthr) s_logit[e] = __ldcg(logits + e);
     group_sync(bar, nthr);
     // two threads per expert: each counts the experts that beat it over half of E
@@ -158,6 +162,10 @@ __device__ inline void route_topk(const float* __restrict__ logits, int E, int k
         const float lmax = __shfl_sync(0xffffffffu, l, 0);
         const float pr = tid < k ? expf(l - lmax) : 0.f;
         float z = pr;
+        if (!renorm) {
+            z = 0.f;
+            for (int e = tid; e < E; e += 32) z += expf(s_logit[e] - lmax);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         if (tid < k) s_w[tid] = pr / z;
@@ -647,11 +655,11 @@ __global__ void __launch_bounds__(NTHREADS) stream_gemv_kernel(const StreamParam
     // this grid was allowed to start; the gate/up kernel reads them right
     // after its own dependency wait.
     if (p.moe && MODE == MODE_DOWN) {
-        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0);
+        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0, p.renorm);
     } else if (p.moe && MODE == MODE_GATEUP) {
         pdl_wait();
         pdl_trigger();
-        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0);
+        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0, p.renorm);
         if (blockIdx.x == 0 && tid < p.topk) {
             if (p.topk_idx_out) p.topk_idx_out[tid] = s_idx[tid];
             if (p.topk_w_out) p.topk_w_out[tid] = s_w[tid];

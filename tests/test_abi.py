@@ -89,6 +89,10 @@ def test_moe_refusals(lib):
     assert call(shape(), ws_bytes=16) == qm.ERR_INVALID_ARGUMENT
     assert call(shape(), ptr=None) == qm.ERR_INVALID_ARGUMENT
     assert "top_k" in qm.last_error() or "null" in qm.last_error()
+    bad = shape()
+    bad.route_flags = 2  # not a known flag
+    assert call(bad) == qm.ERR_INVALID_ARGUMENT
+    assert "route_flags" in qm.last_error()
 
 
 def test_ffn_refusals(lib):

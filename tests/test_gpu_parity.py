@@ -132,7 +132,7 @@ def gpu_moe(qm, inp, shp):
     import torch
     T, K = shp["n_tokens"], shp["top_k"]
     s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], K, T,
-                     shp["gate"], shp["up"], shp["down"])
+                     shp["gate"], shp["up"], shp["down"], shp.get("renormalize", True))
     res = _dev(inp["residual"])
     idx = torch.full((T, K), -1, dtype=torch.int32, device="cuda")
     w = torch.zeros((T, K), device="cuda")
@@ -146,7 +146,8 @@ def gpu_moe(qm, inp, shp):
 def oracle_moe(orc, inp, shp, tokens=None):
     return orc.moe_ffn(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"],
                        shp["gate"], shp["up"], shp["down"], inp["router"], inp["gate"],
-                       inp["up"], inp["down"], inp["x"], inp["residual"], tokens=tokens)
+                       inp["up"], inp["down"], inp["x"], inp["residual"], tokens=tokens,
+                       renormalize=shp.get("renormalize", True))
 
 
 MOE_SMALL = [
@@ -203,6 +204,30 @@ def test_moe_prefill_workload_sampled(qm, orc):
             assert route_is_valid(idx[t], logits[t], scales[t], K), t
             mismatched += list(idx[t]) != list(ri)
     assert mismatched <= 5
+
+
+# ------------------------------------------ routing without renormalisation
+NO_RENORM = [
+    dict(synth.MOE_DECODE),                                                # fused, 1 token
+    dict(synth.MOE_DECODE, n_tokens=5),                                    # batched
+    dict(hidden=256, expert_dim=256, num_experts=8, top_k=2, n_tokens=64,
+         gate=synth.Q4_K, up=synth.Q4_K, down=synth.Q6_K),                 # tensor cores
+    dict(hidden=512, expert_dim=256, num_experts=256, top_k=16, n_tokens=1,
+         gate=synth.Q5_K, up=synth.Q5_K, down=synth.Q8_0),                 # E = 256, k = 16
+]
+
+
+@pytest.mark.parametrize("shp", NO_RENORM, ids=lambda s: "E{num_experts}k{top_k}T{n_tokens}".format(**s))
+def test_moe_no_renorm(qm, orc, shp):
+    """route_flags = QMOE_ROUTE_NO_RENORM: weights are the softmax
+    probabilities of the selected experts; they sum to less than one."""
+    shp = dict(shp, renormalize=False)
+    inp = synth.moe_inputs(41 + shp["n_tokens"], **shp)
+    out, idx, w = gpu_moe(qm, inp, shp)
+    ref = oracle_moe(orc, inp, shp)
+    assert check_moe(out, idx, w, ref) <= 1
+    assert np.all(w.sum(axis=1) < 1.0)
+    assert qm.device_status() == qm.OK
 
 
 # ----------------------------------------------- many tokens (tensor cores)

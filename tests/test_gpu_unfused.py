@@ -21,7 +21,7 @@ def test_separate_kernel_path_parity():
     cmd = [sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_gpu_parity.py"),
            os.path.join(ROOT, "tests", "test_gpu_rmsnorm.py"),
            "-m", "gpu", "-q", "-x", "-p", "no:cacheprovider",
-           "-k", "ffn_small or ffn_dense or moe_small or moe_decode or rmsnorm"]
+           "-k", "ffn_small or ffn_dense or moe_small or moe_decode or rmsnorm or no_renorm"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
