@@ -187,11 +187,17 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  *               overlap on the GPU must not share one
  * Execution: for T >= 32 tokens with Q4_K gate/up and Q6_K down stacks, the
  * tokens are grouped by expert and the expert products run on the tensor
- * cores.  Otherwise each token runs one cooperative kernel (one CTA per SM):
+ * cores.  A single token runs one cooperative kernel (one CTA per SM):
  * router GEMV, a grid barrier, routing in every CTA, the routed gate/up rows
  * and then the down rows streamed through one pipeline, a second grid barrier
- * before the down products.  QMOE_FUSED=0 (see ffn_swiglu) replaces that
- * kernel by three launches per token.
+ * before the down products.  2..31 tokens run in cooperative launches of up
+ * to 16 tokens (fewer where the layer's tiles and x' tables need more shared
+ * memory): every CTA routes all the launch's tokens and groups them by
+ * expert, each routed expert's gate/up rows are staged once for all its
+ * tokens, and the down products run per token as in the single-token kernel.
+ * QMOE_BATCH=0 (read once per process) runs those tokens one launch each;
+ * QMOE_FUSED=0 (see ffn_swiglu) replaces the single-token kernel by three
+ * launches per token and also disables the batched launches.
  * Errors: INVALID_ARGUMENT (null, shape fields out of range, k > E, small
  * workspace, misalignment), UNSUPPORTED (E > 256, k > 16, F32 or mixed
  * gate/up formats, sizes not multiples of 256), CUDA. */
