@@ -55,7 +55,8 @@ struct BatchParams {
 
 struct BatchLayout {
     int off_full, off_empty, off_ridx, off_rw, off_mask, off_slot, off_act, off_start, off_ptok,
-        off_pw, off_porig, off_inv, off_red, off_part, off_xs, off_xq, off_stage, total;
+        off_pw, off_porig, off_inv, off_red, off_rpart, off_part, off_xs, off_xq, off_stage,
+        total;
 };
 
 // Groups of 256 the x' region holds: every token's input (gate/up) or one
@@ -81,6 +82,7 @@ __host__ __device__ inline BatchLayout batch_layout(const BatchParams& b) {
     L.off_porig = o; o += 4 * MAX_PAIRS;
     L.off_inv = o;   o += 4 * TB_MAX;
     L.off_red = o;   o += 4 * NCW * TB_MAX;
+    L.off_rpart = o; o += 4 * TB_MAX * (32768 / 512);
     L.off_part = o;  o += 4 * 2 * b.T * NCW * MAX_ROWS;
     const int ng = batch_table_groups(b);
     o = align_up(o, 16);
@@ -327,6 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     int32_t* s_porig = reinterpret_cast<int32_t*>(smem + L.off_porig);
     float* s_inv = reinterpret_cast<float*>(smem + L.off_inv);
     float* red = reinterpret_cast<float*>(smem + L.off_red);
+    float* rpart = reinterpret_cast<float*>(smem + L.off_rpart);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
     float* xq = reinterpret_cast<float*>(smem + L.off_xq);
@@ -396,13 +399,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
         }
         named_bar(1, NC);
     }
-    // x' tables of every token for the gate/up phase
+    // x' tables of every token for the gate/up phase; with H a multiple of
+    // 512 the same pass forms the logits of this CTA's first expert
+    const bool rmerge = (H % 512) == 0 && cta < E;
     build_xprime<FmtG, 2>(b.x, T * (H / 256), xq, xs, tid, NC, b.norm_w, 1.f,
-                       b.norm_w ? s_inv : nullptr, H / 16);
-    // logits of this CTA's experts for every token
+                          b.norm_w ? s_inv : nullptr, H / 16,
+                          rmerge ? b.router + static_cast<int64_t>(cta) * H : nullptr, rpart);
+    if (rmerge) {
+        named_bar(1, NC);
+        if (tid < T) {
+            float sum = 0.f;
+            for (int j = 0; j < H / 512; ++j) sum += rpart[tid * (H / 512) + j];
+            b.logits[static_cast<int64_t>(tid) * E + cta] = sum;
+        }
+    }
+    // logits of this CTA's (other) experts for every token
     {
         const float4* n4 = reinterpret_cast<const float4*>(b.norm_w);
-        for (int e = cta; e < E; e += ncta) {
+        for (int e = rmerge ? cta + ncta : cta; e < E; e += ncta) {
             const float4* r4 = reinterpret_cast<const float4*>(b.router + static_cast<int64_t>(e) * H);
             float acc[TB_MAX];
 #pragma unroll

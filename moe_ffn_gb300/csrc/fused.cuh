@@ -47,8 +47,8 @@ struct FusedParams {
 };
 
 struct FusedLayout {
-    int off_full, off_empty, off_tidx, off_tw, off_logit, off_red, off_part, off_xs, off_xq,
-        off_stage, total;
+    int off_full, off_empty, off_tidx, off_tw, off_logit, off_red, off_rpart, off_part, off_xs,
+        off_xq, off_stage, total;
 };
 
 __host__ __device__ inline FusedLayout fused_layout(const FusedParams& f) {
@@ -60,6 +60,7 @@ __host__ __device__ inline FusedLayout fused_layout(const FusedParams& f) {
     L.off_tw = o;    o += 4 * MAX_TOPK;
     L.off_logit = o; o += 4 * MAX_EXPERTS;
     L.off_red = o;   o += 4 * NCW;
+    L.off_rpart = o; o += 4 * (32768 / 512);
     L.off_part = o;  o += 4 * 2 * NCW * MAX_ROWS;
     const int ng_gu = f.gu.nb_seg * f.gu.n_kseg, ng_dn = f.dn.nb_seg * f.dn.n_kseg;
     const int ng = ng_gu > ng_dn ? ng_gu : ng_dn;  // the down x' reuses the gate/up table
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
     float* s_w = reinterpret_cast<float*>(smem + L.off_tw);
     float* s_logit = reinterpret_cast<float*>(smem + L.off_logit);
     float* red = reinterpret_cast<float*>(smem + L.off_red);
+    float* rpart = reinterpret_cast<float*>(smem + L.off_rpart);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
     float* xq = reinterpret_cast<float*>(smem + L.off_xq);
@@ -209,11 +211,22 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
     // ffn_norm (optional): every CTA reads the whole hidden state anyway
     const float inv =
         f.norm_w ? rms_inverse(f.gu.x, f.gu.nb_seg * 256, f.eps, red, tid, NC, 1) : 1.f;
-    build_xprime<FmtG>(f.gu.x, f.gu.nb_seg, xq, xs, tid, NC, f.norm_w, inv);
+    // with H a multiple of 512 the x' pass also forms this CTA's first logit
+    const bool rmerge = f.moe && (f.H % 512) == 0 && cta < f.E;
+    build_xprime<FmtG, 2>(f.gu.x, f.gu.nb_seg, xq, xs, tid, NC, f.norm_w, inv, nullptr,
+                          f.H / 16, rmerge ? f.router + cta * f.H : nullptr, rpart);
     if (f.moe) {
-        // logits of this CTA's experts: e = cta, cta + ncta, ...
+        if (rmerge) {
+            named_bar(1, NC);
+            if (tid == 0) {
+                float sum = 0.f;
+                for (int j = 0; j < f.H / 512; ++j) sum += rpart[j];
+                f.logits[cta] = sum;
+            }
+        }
+        // logits of this CTA's (other) experts: e = cta, cta + ncta, ...
         const float4* x4 = reinterpret_cast<const float4*>(f.gu.x);
-        for (int64_t e = cta; e < f.E; e += ncta) {
+        for (int64_t e = rmerge ? cta + ncta : cta; e < f.E; e += ncta) {
             const float4* r4 = reinterpret_cast<const float4*>(f.router + e * f.H);
             float acc = 0.f;
             const float4* n4 = reinterpret_cast<const float4*>(f.norm_w);

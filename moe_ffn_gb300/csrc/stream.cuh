@@ -201,7 +201,9 @@ template <class Fmt, int UNR = 4>
 __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, float* xq,
                                     float* xs, int tid, int nthreads,
                                     const float* __restrict__ nw = nullptr, float inv = 1.f,
-                                    const float* inv_tok = nullptr, int tok_n16 = 0) {
+                                    const float* inv_tok = nullptr, int tok_n16 = 0,
+                                    const float* __restrict__ rrow = nullptr,
+                                    float* rpart = nullptr) {
     // x' in the per-quarter interleaved order; xs = sum of x per 16 elements.
     // A thread takes 16-element chunks of x: it loads the chunk's four
     // aligned float4s (all loads in flight before any use, so the table
@@ -212,25 +214,36 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
     // With inv_tok, x holds several tokens of tok_n16 chunks each, token t
     // normed with inv_tok[t] (nw applies per token).  UNR chunks per thread
     // are in flight at once.
+    // With rrow (one f32 router row), the same pass forms the router dot
+    // product of every token: the row's chunk is loaded beside the token's,
+    // and each warp's 32 chunks (one token: tok_n16 and nthreads multiples
+    // of 32) leave one partial in rpart[t * tok_n16 / 32 + chunk / 32], to be
+    // summed in that order.
     const int n16 = ngroups * 16;
     const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* r4 = reinterpret_cast<const float4*>(rrow);
     float4* xq4 = reinterpret_cast<float4*>(xq);
     for (int base = tid; base < n16; base += nthreads * UNR) {
         float4 v[UNR][4];
+        float4 rv[UNR][4];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
             const int c = base + u * nthreads;
             if (c < n16) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[u][k] = __ldcg(x4 + 4 * c + k);
+                int cw = c;
+                float iv = inv;
+                if (inv_tok || rrow) {
+                    const int tk = c / tok_n16;
+                    cw = c - tk * tok_n16;
+                    if (inv_tok) iv = inv_tok[tk];
+                }
+                if (rrow) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) rv[u][k] = __ldg(r4 + 4 * cw + k);
+                }
                 if (nw) {
-                    int cw = c;
-                    float iv = inv;
-                    if (inv_tok) {
-                        const int tk = c / tok_n16;
-                        cw = c - tk * tok_n16;
-                        iv = inv_tok[tk];
-                    }
                     const float4* w4 = reinterpret_cast<const float4*>(nw);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -246,6 +259,19 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
             const int c = base + u * nthreads;
+            if (rrow && c - (c & 31) < n16) {  // whole warps: all lanes valid
+                float d = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    d = fmaf(rv[u][k].x, v[u][k].x, d);
+                    d = fmaf(rv[u][k].y, v[u][k].y, d);
+                    d = fmaf(rv[u][k].z, v[u][k].z, d);
+                    d = fmaf(rv[u][k].w, v[u][k].w, d);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                if ((c & 31) == 0) rpart[c >> 5] = d;
+            }
             if (c < n16) {
                 float s = 0.f;
 #pragma unroll
