@@ -191,7 +191,7 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  * router GEMV, a grid barrier, routing in every CTA, the routed gate/up rows
  * and then the down rows streamed through one pipeline, a second grid barrier
  * before the down products.  2..31 tokens run in cooperative launches of up
- * to 16 tokens (fewer where the layer's tiles and x' tables need more shared
+ * to 16 tokens (fewer where the layer's tiles and x tables need more shared
  * memory): every CTA routes all the launch's tokens and groups them by
  * expert, each routed expert's gate/up rows are staged once for all its
  * tokens, and the down products run per token as in the single-token kernel.

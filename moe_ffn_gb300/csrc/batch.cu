@@ -9,7 +9,7 @@
 namespace qmoe {
 
 // One stage must hold a whole gate/up tile (32 rows); the down phase is
-// chunked as the batch-1 kernel's.  Two stages and the x' tables must fit.
+// chunked as the batch-1 kernel's.  Two stages and the x tables must fit.
 template <class FmtG, class FmtD>
 static bool plan_batch(BatchParams& b, int smem_optin, int* smem_bytes) {
     b.gu.stage_bytes = b.dn.stage_bytes = 0;

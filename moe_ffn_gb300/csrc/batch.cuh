@@ -26,8 +26,8 @@
 // The producer warp streams the gate/up tiles and then the down tiles of the
 // CTA through one ring, as in the batch-1 fused kernel.
 //
-// x' tables: phase 3 keeps one per token (T * H floats); phase 4 builds the
-// table of one token's activations (k * F floats) when the CTA's down units
+// x tables: phase 3 keeps one per token (T * H int16); phase 4 builds the
+// table of one token's activations (k * F values) when the CTA's down units
 // reach that token.  Gate/up tiles hold whole rows (one chunk per tile).
 #pragma once
 #include "fused.cuh"
@@ -59,7 +59,7 @@ struct BatchLayout {
         total;
 };
 
-// Groups of 256 the x' region holds: every token's input (gate/up) or one
+// Groups of 256 the x region holds: every token's input (gate/up) or one
 // token's k activation rows (down).
 __host__ __device__ inline int batch_table_groups(const BatchParams& b) {
     const int gu = b.T * (b.H / 256), dn = b.topk * (b.F / 256);
@@ -86,9 +86,9 @@ __host__ __device__ inline BatchLayout batch_layout(const BatchParams& b) {
     L.off_part = o;  o += 4 * 2 * b.T * NCW * MAX_ROWS;
     const int ng = batch_table_groups(b);
     o = align_up(o, 16);
-    L.off_xs = o;    o += 4 * 16 * ng;
+    L.off_xs = o;    o += XS_GROUP_BYTES * ng;
     o = align_up(o, 128);
-    L.off_xq = o;    o += 4 * 256 * ng;
+    L.off_xq = o;    o += XQ_GROUP_BYTES * ng;
     o = align_up(o, 128);
     L.off_stage = o; o += b.gu.stage_bytes * b.gu.nstages;
     o += 16;  // tail slack (see smem_layout)
@@ -180,17 +180,17 @@ struct PairLists {
 // For every pair (t, s) of the tile's expert: act[t][s][f] = w * silu(g) * u.
 template <class Fmt>
 __device__ bool consume_batch_gateup(const StreamParams& p, const Ring& ring, const PairLists& pl,
-                                     const float* xq, const float* xs, float* part, int T,
+                                     const uint32_t* xq, const float* xs, float* part, int T,
                                      float* act, int64_t ubeg, int64_t uend, int& it, int tid) {
     using G = ModeGeom<MODE_GATEUP>;
     constexpr int R = G::R;
     const int v = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
-    const float4* xq4 = reinterpret_cast<const float4*>(xq);
+    const uint4* xq4 = reinterpret_cast<const uint4*>(xq);
     const int ntiles = static_cast<int>((uend - ubeg) / G::TU);
     const int nb = p.nb_seg;
     bool ok = true;
-    float x[64];
+    uint32_t x[32];
     for (int t = 0; t < ntiles; ++t) {
         const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
         const int a = tile_slot<MODE_GATEUP>(p, u0);
@@ -229,11 +229,12 @@ __device__ bool consume_batch_gateup(const StreamParams& p, const Ring& ring, co
             if (ok) {
                 for (int b = v; b < nb; b += G::WK) {
                     const int gidx = tok * nb + b;
-                    load_xq(xq4 + gidx * 64, q, x);
+                    load_xq(xq4 + gidx * 32, q, x);
                     const uint8_t* sbp[R];
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr) sbp[rr] = sbp0[rr] + b * Fmt::SBB;
-                    Fmt::template dotR<R>(sbp, q, x, xs + gidx * 16, acc);
+                    const float* xsg = xs + gidx * XS_GROUP_FLOATS;
+                    Fmt::template dotR<R>(sbp, q, x, xsg, xsg + 16, acc);
                 }
             }
 #pragma unroll
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     float* rpart = reinterpret_cast<float*>(smem + L.off_rpart);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
-    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
+    uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.off_xq);
     __shared__ int s_abort, s_nact;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
         }
         named_bar(1, NC);
     }
-    // x' tables of every token for the gate/up phase; with H a multiple of
+    // x tables of every token for the gate/up phase; with H a multiple of
     // 512 the same pass forms the logits of this CTA's first expert
     const bool rmerge = (H % 512) == 0 && cta < E;
     build_xprime<FmtG, 2>(b.x, T * (H / 256), xq, xs, tid, NC, b.norm_w, 1.f,
@@ -550,7 +551,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
         if (tid == 0) sync_invalidate(b.sync);
         return;
     }
-    // down, token by token: the x' table of the token's k activation rows,
+    // down, token by token: the x table of the token's k activation rows,
     // then its rows of this CTA through the batch-1 down consumer
     int64_t db, de;
     tile_range(static_cast<int64_t>(T) * H, cta, ncta, db, de);

@@ -63,11 +63,11 @@ __host__ __device__ inline FusedLayout fused_layout(const FusedParams& f) {
     L.off_rpart = o; o += 4 * (32768 / 512);
     L.off_part = o;  o += 4 * 2 * NCW * MAX_ROWS;
     const int ng_gu = f.gu.nb_seg * f.gu.n_kseg, ng_dn = f.dn.nb_seg * f.dn.n_kseg;
-    const int ng = ng_gu > ng_dn ? ng_gu : ng_dn;  // the down x' reuses the gate/up table
+    const int ng = ng_gu > ng_dn ? ng_gu : ng_dn;  // the down x table reuses the gate/up region
     o = align_up(o, 16);
-    L.off_xs = o;    o += 4 * 16 * ng;
+    L.off_xs = o;    o += XS_GROUP_BYTES * ng;
     o = align_up(o, 128);
-    L.off_xq = o;    o += 4 * 256 * ng;
+    L.off_xq = o;    o += XQ_GROUP_BYTES * ng;
     o = align_up(o, 128);
     L.off_stage = o; o += f.gu.stage_bytes * f.gu.nstages;
     o += 16;  // tail slack (see smem_layout)
@@ -152,7 +152,7 @@ __device__ __forceinline__ void sync_close(unsigned long long* sync) {
 }
 
 template <class FmtG, class FmtD>
-__global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f) {
+__global__ void __launch_bounds__(NTHREADS, 1) fused_ffn_kernel(const FusedParams f) {
     extern __shared__ __align__(128) uint8_t smem[];
     const FusedLayout L = fused_layout(f);
     Ring ring;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
     float* rpart = reinterpret_cast<float*>(smem + L.off_rpart);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
-    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
+    uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.off_xq);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
     // ffn_norm (optional): every CTA reads the whole hidden state anyway
     const float inv =
         f.norm_w ? rms_inverse(f.gu.x, f.gu.nb_seg * 256, f.eps, red, tid, NC, 1) : 1.f;
-    // with H a multiple of 512 the x' pass also forms this CTA's first logit
+    // with H a multiple of 512 the x-table pass also forms this CTA's first logit
     const bool rmerge = f.moe && (f.H % 512) == 0 && cta < f.E;
     build_xprime<FmtG, 2>(f.gu.x, f.gu.nb_seg, xq, xs, tid, NC, f.norm_w, inv, nullptr,
                           f.H / 16, rmerge ? f.router + cta * f.H : nullptr, rpart);
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(NTHREADS) fused_ffn_kernel(const FusedParams f
         }
         named_bar_arrive(2, NTHREADS);  // the producer may stream the routed experts
     } else {
-        named_bar(1, NC);  // x' complete
+        named_bar(1, NC);  // x table complete
         if (s_abort) {
             if (tid == 0) sync_invalidate(f.sync);
             return;

@@ -158,7 +158,7 @@ static bool plan(StreamParams& p, int smem_optin, int grid, int* smem_bytes) {
     // A CTA with a single tile gains nothing from a ring: one stage may then
     // hold the whole tile (whole rows, so few and large copies).  Otherwise
     // the stage budget is at most 96 KB, and two stages must fit beside the
-    // x' table.
+    // x table.
     const int64_t per_cta = (p.units + grid - 1) / grid;
     const bool one_tile = per_cta <= G::TU;
     bool planned = false;

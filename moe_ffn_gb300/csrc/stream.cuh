@@ -7,8 +7,8 @@
 // mbarrier).  Warps 0..7 are consumers.  A tile holds 8*R row slots; lane
 // (g = lane/4, q = lane%4) owns slots rr*8 + g (rr < R) and quarter q of each
 // 256-element group its warp is given: warp v takes groups v, v+8, ... of
-// the chunk.  A lane loads its 64 x' values of a group into registers once
-// and applies them to its R rows.  Per-row partial sums are reduced by
+// the chunk.  A lane loads its 32 x registers of a group (64 activations as
+// 16-bit integers, formats.cuh) once and applies them to its R rows.  Per-row partial sums are reduced by
 // shuffles across the four quarters and through shared memory across warps,
 // in a fixed order (deterministic).
 //
@@ -80,7 +80,14 @@ template <int MODE> struct ModeGeom {
     static constexpr int WK = NCW;                         // warps along K
 };
 
-// Shared-memory carve-up (dynamic): [barriers][topk][part][xs16][xq][stages]
+// The x table of one 256-element group: 32 x registers per quarter lane
+// (int16 pairs, uint4 [8][4]), and beside it in the xs region 16 sums of x
+// (one per 16 elements) then the 8 block scales.
+constexpr int XQ_GROUP_BYTES = 512;
+constexpr int XS_GROUP_FLOATS = 24;
+constexpr int XS_GROUP_BYTES = 4 * XS_GROUP_FLOATS;
+
+// Shared-memory carve-up (dynamic): [barriers][topk][part][xs][xq][stages]
 struct SmemLayout {
     int off_full, off_empty, off_tidx, off_tw, off_logit, off_part, off_xs, off_xq, off_stage,
         total;
@@ -98,9 +105,9 @@ __host__ __device__ inline SmemLayout smem_layout(const StreamParams& p) {
     L.off_logit = o; o += 4 * MAX_EXPERTS;
     L.off_part = o;  o += 4 * 2 * NCW * MAX_ROWS;
     o = align_up(o, 16);
-    L.off_xs = o;    o += 4 * 16 * p.nb_seg * p.n_kseg;
+    L.off_xs = o;    o += XS_GROUP_BYTES * p.nb_seg * p.n_kseg;
     o = align_up(o, 128);
-    L.off_xq = o;    o += 4 * 256 * p.nb_seg * p.n_kseg;
+    L.off_xq = o;    o += XQ_GROUP_BYTES * p.nb_seg * p.n_kseg;
     o = align_up(o, 128);
     L.off_stage = o; o += p.stage_bytes * p.nstages;
     o += 16;  // tail slack: a Q6_K lane's word loads reach <= 2 bytes past a super-block
@@ -198,18 +205,21 @@ __device__ inline float rms_inverse(const float* __restrict__ h, int n, float ep
 }
 
 template <class Fmt, int UNR = 4>
-__device__ inline void build_xprime(const float* __restrict__ x, int ngroups, float* xq,
+__device__ inline void build_xprime(const float* __restrict__ x, int ngroups, uint32_t* xq,
                                     float* xs, int tid, int nthreads,
                                     const float* __restrict__ nw = nullptr, float inv = 1.f,
                                     const float* inv_tok = nullptr, int tok_n16 = 0,
                                     const float* __restrict__ rrow = nullptr,
                                     float* rpart = nullptr) {
-    // x' in the per-quarter interleaved order; xs = sum of x per 16 elements.
-    // A thread takes 16-element chunks of x: it loads the chunk's four
-    // aligned float4s (all loads in flight before any use, so the table
-    // costs one L2 round trip), stores their sum to xs, and scatters each
-    // float4 to its x' slot (the formats' element orders keep every slot
-    // four consecutive elements), each element scaled by its own power of two.
+    // The x table (see formats.cuh): x as 16-bit integers in the lanes'
+    // register order, one scale per 32-element block (max |x| / 32767; NaN if
+    // the block holds a non-finite value, so that it reaches the result), and
+    // the f32 sum of x per 16 elements.  A thread takes 16-element chunks of
+    // x: it loads the chunk's four aligned float4s (all loads in flight
+    // before any use, so the table costs one L2 round trip), takes the block
+    // maximum with its neighbour (the chunk pair 2m, 2m+1 is block m),
+    // rounds, and scatters each granule of four to its slot (the formats'
+    // element orders keep every slot four consecutive elements).
     // With nw, the table is of the normed input x_j * inv * nw_j (ffn_norm).
     // With inv_tok, x holds several tokens of tok_n16 chunks each, token t
     // normed with inv_tok[t] (nw applies per token).  UNR chunks per thread
@@ -222,8 +232,11 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
     const int n16 = ngroups * 16;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const float4* r4 = reinterpret_cast<const float4*>(rrow);
-    float4* xq4 = reinterpret_cast<float4*>(xq);
-    for (int base = tid; base < n16; base += nthreads * UNR) {
+    uint2* xq2 = reinterpret_cast<uint2*>(xq);
+    // warps step together (the shuffles below need every lane of the warp,
+    // also those whose chunks are past the end): nthreads is a multiple of 32
+    for (int wbase = tid & ~31; wbase < n16; wbase += nthreads * UNR) {
+        const int base = wbase + (tid & 31);
         float4 v[UNR][4];
         float4 rv[UNR][4];
 #pragma unroll
@@ -254,6 +267,9 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
                         v[u][k].w *= iv * wv.w;
                     }
                 }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 #pragma unroll
@@ -272,22 +288,39 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
                 for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
                 if ((c & 31) == 0) rpart[c >> 5] = d;
             }
+            // block maximum over this chunk and its neighbour (lane ^ 1)
+            float mx = 0.f;
+            bool bad = false;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float a0 = fabsf(v[u][k].x), a1 = fabsf(v[u][k].y), a2 = fabsf(v[u][k].z),
+                            a3 = fabsf(v[u][k].w);
+                mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+                bad = bad || !(a0 <= 3.402823466e38f) || !(a1 <= 3.402823466e38f) ||
+                      !(a2 <= 3.402823466e38f) || !(a3 <= 3.402823466e38f);
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            bad = __shfl_xor_sync(0xffffffffu, static_cast<int>(bad), 1) != 0 || bad;
             if (c < n16) {
+                const float qs = (bad || mx == 0.f) ? 0.f : 32767.f / mx;
                 float s = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) s += (v[u][k].x + v[u][k].y) + (v[u][k].z + v[u][k].w);
-                xs[c] = s;
                 const int g = c >> 4;
+                xs[g * XS_GROUP_FLOATS + (c & 15)] = s;
+                if ((c & 1) == 0)
+                    xs[g * XS_GROUP_FLOATS + 16 + ((c & 15) >> 1)] =
+                        bad ? __int_as_float(0x7FC00000) : mx * (1.0f / 32767.f);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int slot = Fmt::xslot(4 * (c & 15) + k);
-                    const int q = slot & 3, i = 4 * (slot >> 2);
-                    float4 o;
-                    o.x = v[u][k].x * xprime_scale(Fmt::pos(q, i));
-                    o.y = v[u][k].y * xprime_scale(Fmt::pos(q, i + 1));
-                    o.z = v[u][k].z * xprime_scale(Fmt::pos(q, i + 2));
-                    o.w = v[u][k].w * xprime_scale(Fmt::pos(q, i + 3));
-                    xq4[g * 64 + slot] = o;
+                    const int q = slot & 3, i4 = slot >> 2;
+                    const uint32_t e0 = static_cast<uint16_t>(__float2int_rn(v[u][k].x * qs));
+                    const uint32_t e1 = static_cast<uint16_t>(__float2int_rn(v[u][k].y * qs));
+                    const uint32_t e2 = static_cast<uint16_t>(__float2int_rn(v[u][k].z * qs));
+                    const uint32_t e3 = static_cast<uint16_t>(__float2int_rn(v[u][k].w * qs));
+                    xq2[(g * 32 + (i4 >> 1) * 4 + q) * 2 + (i4 & 1)] =
+                        make_uint2(e0 | (e1 << 16), e2 | (e3 << 16));
                 }
             }
         }
@@ -511,27 +544,27 @@ __device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int
 
 // Consumer warps 0..NCW-1: reduce every tile of [ubeg, uend) and write the
 // outputs (QMV: y = W.x; GATEUP: a = w * silu(g) * u; DOWN: out += D.a).
-// x' / xs must already hold the phase's input.  False (in every consumer
+// xq / xs must already hold the phase's x table.  False (in every consumer
 // thread alike) if a stage wait timed out: a warp whose wait expired skips
 // the rest of its waits and arithmetic but still takes part in every named
 // barrier, so no warp is left waiting, and no output of a tile is written
 // unless every warp's data for it arrived.
 template <class Fmt, int MODE>
 __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int32_t* s_idx,
-                              const float* s_w, const float* xq, const float* xs, float* part,
+                              const float* s_w, const uint32_t* xq, const float* xs, float* part,
                               int64_t ubeg, int64_t uend, int& it, int tid) {
     using G = ModeGeom<MODE>;
     constexpr int R = G::R;
     const int v = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
-    const float4* xq4 = reinterpret_cast<const float4*>(xq);
+    const uint4* xq4 = reinterpret_cast<const uint4*>(xq);
     const int ntiles = static_cast<int>((uend - ubeg + G::TU - 1) / G::TU);
     bool ok = true;
     // Gate/up tiles with K <= 8 groups give a warp the same group in every
-    // tile: its x' stays in registers.  Elsewhere groups change each call,
-    // and keeping x' live would only cost registers.
+    // tile: its x registers stay loaded.  Elsewhere groups change each call,
+    // and keeping them live would only cost registers.
     constexpr bool KEEP_X = MODE == MODE_GATEUP;
-    float x[64];
+    uint32_t x[32];
     int xg = -1;
     for (int t = 0; t < ntiles; ++t) {
         const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
@@ -575,10 +608,10 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
                 const int ks = cd.ks0 + pk, b = cd.b0 + bb;
                 const int gidx = ks * p.nb_seg + b;
                 if (!KEEP_X || gidx != xg) {
-                    load_xq(xq4 + gidx * 64, q, x);
+                    load_xq(xq4 + gidx * 32, q, x);
                     xg = gidx;
                 }
-                const float* xsg = xs + gidx * 16;
+                const float* xsg = xs + gidx * XS_GROUP_FLOATS;
                 const uint32_t ksoff =
                     (MODE == MODE_DOWN && p.moe)
                         ? static_cast<uint32_t>(s_idx[ks]) * static_cast<uint32_t>(p.es0)
@@ -591,7 +624,7 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
                     const int delta = static_cast<int>((rowlo[rr] + ksoff + b0off) & 15u);
                     sbp[rr] = st + rowoff[rr] + pk * p.piece_stride + delta + bb * Fmt::SBB;
                 }
-                Fmt::template dotR<R>(sbp, q, x, xsg, acc);
+                Fmt::template dotR<R>(sbp, q, x, xsg, xsg + 16, acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ring.empty[s]);
@@ -644,7 +677,7 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
 }
 
 template <class Fmt, int MODE>
-__global__ void __launch_bounds__(NTHREADS) stream_gemv_kernel(const StreamParams p) {
+__global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = smem_layout(p);
     Ring ring;
@@ -658,7 +691,7 @@ __global__ void __launch_bounds__(NTHREADS) stream_gemv_kernel(const StreamParam
     float* s_logit = reinterpret_cast<float*>(smem + L.off_logit);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
-    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
+    uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.off_xq);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int64_t ubeg, uend;
