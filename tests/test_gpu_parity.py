@@ -73,6 +73,35 @@ def test_qmv_sweep_workload(qm, orc, qt):
     check_gemv(y, ref, sabs, f"sweep {QNAME[qt]}")
 
 
+@pytest.mark.parametrize("qt", QTS, ids=lambda q: QNAME[q])
+def test_qmv_wide_range_x(qm, orc, qt):
+    """The activations are rounded to 16 bits per 32-element block.  Blocks
+    whose values span six decades (one value 1e3, the rest ~1e-3, random
+    signs) still meet the stated bound, with margin."""
+    g = synth.rng(900 + qt)
+    rows, cols = 300, 2048
+    W = synth.quant_matrix(g, qt, rows, cols)
+    x = (synth.normal(g, cols) * 1e-3).astype(np.float32)
+    x[g.integers(0, 32, cols // 32) + np.arange(0, cols, 32)] = 1e3 * np.sign(g.standard_normal(cols // 32))
+    y = gpu_qmv(qm, qt, W, rows, cols, x)
+    ref, sabs = orc.matvec(qt, W, rows, cols, x, with_sabs=True)
+    assert check_gemv(y, ref, sabs, f"wide-range x {QNAME[qt]}") < 0.5
+
+
+@pytest.mark.parametrize("qt", QTS, ids=lambda q: QNAME[q])
+def test_qmv_nan_x_reaches_every_row(qm, orc, qt):
+    """A NaN activation makes every output NaN (each row multiplies it), as in
+    the oracle: the rounded block carries a NaN scale."""
+    g = synth.rng(950 + qt)
+    rows, cols = 64, 1024
+    W = synth.quant_matrix(g, qt, rows, cols)
+    x = synth.normal(g, cols)
+    x[517] = np.nan
+    y = gpu_qmv(qm, qt, W, rows, cols, x)
+    ref = orc.matvec(qt, W, rows, cols, x)
+    assert np.all(np.isnan(ref)) and np.all(np.isnan(y))
+
+
 def test_qmv_repeatable_and_in_stream_order(qm, orc):
     """Back-to-back calls on one stream with a dependent x: y2 = W (y1[:cols])."""
     import torch
