@@ -32,9 +32,14 @@
  *     blocks, row_bytes = cols / block_elems * block_bytes.  W must be 16-byte
  *     aligned; the kernels read whole 16-byte granules that contain W's bytes
  *     (never a byte outside those granules).
- *   - Floating-point results are f32, accumulated in f32 with FMA; they match
- *     the exact result within |err| <= 1e-3 * sum_j |w_ij x_j| + 1e-6 per GEMV
- *     output, NaN where the exact computation is NaN (a NaN scale).  Non-finite
+ *   - Floating-point results are f32.  The quantized products take the
+ *     activations as 16-bit integers with one f32 scale per 32 elements (max |x|
+ *     of the block / 32767) and sum quants times activations exactly in 32-bit
+ *     integers per sub-block; scales, mins and everything after them are f32
+ *     with FMA.  Results match the exact result within
+ *     |err| <= 1e-3 * sum_j |w_ij x_j| + 1e-6 per GEMV output (the rounding of x
+ *     adds at most sum_j |w_ij| * max |x| of j's block / 65534), NaN where the
+ *     exact computation is NaN (a NaN scale or a NaN activation).  Non-finite
  *     inputs (Inf scales, non-finite x) give non-finite outputs, NaN or Inf.
  *   - Errors: the status names the class; qmoe_last_error() gives a message
  *     (thread-local) naming the refused argument.
