@@ -42,6 +42,20 @@ def test_row_bytes(lib):
     assert qm.row_bytes(99, 256) == -1
 
 
+def test_workspace_sizes_cover_batched_launches(lib):
+    """2..31 tokens run in batched launches of up to 16 tokens, whose
+    activations are [tokens][k][F] f32: the workspace grows with T up to 16
+    tokens' worth and covers the logits of every token."""
+    H, F, E, K = 2048, 768, 128, 8
+    prev = 0
+    for T in (1, 2, 3, 8, 16, 17, 31):
+        s = qm.moe_shape(H, F, E, K, T, qm.Q4_K, qm.Q4_K, qm.Q6_K)
+        need = qm.moe_ffn_workspace_size(s)
+        assert need >= 256 + T * E * 4 + min(T, 16) * K * F * 4
+        assert need % 256 == 0 and need >= prev
+        prev = need
+
+
 def test_workspace_sizes(lib):
     s = qm.moe_shape(2048, 768, 128, 8, 1, qm.Q4_K, qm.Q4_K, qm.Q6_K)
     assert qm.moe_ffn_workspace_size(s) >= 128 * 4 + 8 * 768 * 4
