@@ -28,7 +28,11 @@ sys.path.insert(0, ROOT)
 METRIC = "quantized GEMV weight GB/s & % of HBM peak; MoE FFN layer µs/token"
 FORMATS = [("Q8_0", 1), ("Q4_0", 2), ("Q4_K", 3), ("Q5_K", 4), ("Q6_K", 5)]
 ROWS = COLS = 4096
-L2_BYTES = 129 * 1024 * 1024
+
+
+def l2_bytes(torch, dev):
+    """L2 size of the device, queried at run time."""
+    return int(torch.cuda.get_device_properties(dev).L2_cache_size)
 
 
 def load_peaks():
@@ -146,7 +150,8 @@ def run_ours(args, rank, world):
         mats[name] = (qt, torch.from_numpy(W).to(dev), torch.from_numpy(x).to(dev))
         bytes_w[name] = W.nbytes
     set_bytes = sum(bytes_w.values())
-    n_copies = int(np.ceil(4 * L2_BYTES / set_bytes)) + 1
+    L2 = l2_bytes(torch, dev)
+    n_copies = int(np.ceil(4 * L2 / set_bytes)) + 1
     copies = {n: [mats[n][1].clone() for _ in range(n_copies)] for n, _ in FORMATS}
     ys = {n: torch.empty(ROWS, device=dev) for n, _ in FORMATS}
     torch.cuda.synchronize()
@@ -318,9 +323,9 @@ def load_traffic(key):
 
 
 def layer_launches(separate):
-    """Kernel launches per FFN layer / MoE token: one fused cooperative launch,
-    or `separate` when QMOE_FUSED=0 selects the separate-kernel form."""
-    return separate if os.environ.get("QMOE_FUSED", "1").startswith("0") else 1
+    """Kernel launches per FFN layer / MoE token: one fused cooperative launch
+    (the bench never selects the separate-kernel form)."""
+    return 1
 
 
 def bench_layers(qm, synth, dev, stream, args):

@@ -136,9 +136,8 @@ size_t ffn_swiglu_workspace_size(int64_t hidden, int64_t inter);
  * The layer runs as one cooperative kernel (one CTA per SM): the gate/up
  * rows and then the down rows stream through one pipeline, and a grid
  * barrier orders the activations between the two products.  A layer that does
- * not fit that kernel's shared memory runs as two kernels instead.  Setting
- * the environment variable QMOE_FUSED=0 (read once per process) forces the
- * two-kernel form, for diagnostics. */
+ * not fit that kernel's shared memory runs as two kernels instead, and
+ * qmoe_set_exec_mode(QMOE_EXEC_SEPARATE) forces that form (diagnostics). */
 qmoe_status ffn_swiglu(const void* gate, const void* up, const void* down, int gate_qtype,
                        int up_qtype, int down_qtype, int64_t hidden, int64_t inter,
                        const float* x, float* residual, void* ws, size_t ws_bytes, void* stream);
@@ -200,9 +199,16 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  * memory): every CTA routes all the launch's tokens and groups them by
  * expert, each routed expert's gate/up rows are staged once for all its
  * tokens, and the down products run per token as in the single-token kernel.
- * QMOE_BATCH=0 (read once per process) runs those tokens one launch each;
- * QMOE_FUSED=0 (see ffn_swiglu) replaces the single-token kernel by three
- * launches per token and also disables the batched launches.
+ * qmoe_set_exec_mode selects the forms these kernels replace, for
+ * diagnostics: QMOE_EXEC_UNBATCHED runs 2..31 tokens one launch each,
+ * QMOE_EXEC_SEPARATE runs every token as three launches (router, gate/up,
+ * down).
+ * Routing of non-finite logits: experts are ranked on a total order (NaN
+ * above +Inf above finite values above -Inf, ties to the lower index), so
+ * every one of the k slots names an expert in [0, E).  When a token's
+ * largest logit is not finite (a NaN or +Inf logit, or all logits -Inf) its
+ * softmax is NaN throughout; the route is then experts 0..k-1 with NaN
+ * weights and the token's residual becomes NaN.
  * Errors: INVALID_ARGUMENT (null, shape fields out of range, k > E, small
  * workspace, misalignment), UNSUPPORTED (E > 256, k > 16, F32 or mixed
  * gate/up formats, sizes not multiples of 256), CUDA. */
@@ -265,10 +271,36 @@ qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: QMOE_ERR_TIMEOUT if a bounded device wait expired since the last
- * read (a pipeline stage, or a grid barrier that not every CTA reached); QMOE_ERR_UNSUPPORTED if the many-token MoE path met a decoded gate/up
+ * read (a pipeline stage, or a grid barrier that not every CTA reached);
+ * QMOE_ERR_UNSUPPORTED if the many-token MoE path met a decoded gate/up
  * weight outside f16 range (its output is then not valid); QMOE_ERR_CUDA if
- * the stream reported an error; else QMOE_OK. */
+ * the stream reported an error, or if an internal invariant of the routing
+ * failed (an expert index outside [0, E) was clamped to 0); else QMOE_OK. */
 qmoe_status qmoe_device_status(void* stream);
+
+/* Execution modes for qmoe_set_exec_mode. */
+#define QMOE_EXEC_DEFAULT 0   /* the fused and batched kernels */
+#define QMOE_EXEC_SEPARATE 1  /* every layer / token as separate kernels */
+#define QMOE_EXEC_UNBATCHED 2 /* 2..31 tokens one fused launch each */
+
+/* Diagnostics and tests: selects, for the whole process and every later
+ * call, which of the equivalent kernel forms ffn_swiglu and moe_ffn (and
+ * their _rmsnorm and _noalloc variants) launch.  All forms compute the same
+ * function.  The pages have no counterpart (their layer always runs as
+ * separate launches).  INVALID_ARGUMENT for an unknown mode. */
+qmoe_status qmoe_set_exec_mode(int mode);
+
+/* Tests of the failure path only: on the current device, every bounded
+ * device wait gives up after wait_limit_ns (0 restores the default, 2 s),
+ * and, if skip_arrive_cta >= 0, that CTA of the cooperative layer kernels
+ * never arrives at their grid barriers, so the other CTAs' waits run out:
+ * the kernels then record QMOE_ERR_TIMEOUT (qmoe_device_status) and return
+ * without writing the layer's output.  (-1, 0) restores normal operation.
+ * Synchronises the device before writing the setting.  Errors: CUDA,
+ * UNSUPPORTED (not sm_103), INVALID_ARGUMENT (skip_arrive_cta < -1).  The
+ * pages have no counterpart; their CudaError model ("refuse, never compute
+ * something else") is what the failure path follows. */
+qmoe_status qmoe_set_fault_injection(uint64_t wait_limit_ns, int skip_arrive_cta);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* qmoe_last_error(void);

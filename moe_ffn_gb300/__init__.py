@@ -115,6 +115,8 @@ SIGNATURES = {
     "moe_ffn_rmsnorm": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(_Shape), _P, ctypes.c_float,
                                        _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qmoe_device_status": (ctypes.c_int, [_P]),
+    "qmoe_set_exec_mode": (ctypes.c_int, [ctypes.c_int]),
+    "qmoe_set_fault_injection": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_int]),
     "qmoe_last_error": (ctypes.c_char_p, []),
     "qmoe_row_bytes": (_I64, [ctypes.c_int, _I64]),
 }
@@ -251,6 +253,23 @@ def moe_ffn_noalloc(router_W, gate_stack, up_stack, down_stack, shape: _Shape, x
     _check(lib().moe_ffn_noalloc(_ptr(router_W), _ptr(gate_stack), _ptr(up_stack),
                                  _ptr(down_stack), ctypes.byref(shape), _ptr(x), _ptr(residual),
                                  _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+# qmoe_set_exec_mode
+EXEC_DEFAULT, EXEC_SEPARATE, EXEC_UNBATCHED = 0, 1, 2
+
+
+def set_exec_mode(mode: int) -> None:
+    """Diagnostics and tests: which equivalent kernel forms later calls launch
+    (EXEC_DEFAULT, EXEC_SEPARATE or EXEC_UNBATCHED; see include/qmoe.h)."""
+    _check(lib().qmoe_set_exec_mode(mode))
+
+
+def set_fault_injection(wait_limit_ns: int = 0, skip_arrive_cta: int = -1) -> None:
+    """Failure-path tests only: shorten every bounded device wait and make one
+    CTA of the cooperative kernels skip its grid-barrier arrivals; (0, -1)
+    restores normal operation (see include/qmoe.h)."""
+    _check(lib().qmoe_set_fault_injection(wait_limit_ns, skip_arrive_cta))
 
 
 def device_status(stream=None) -> int:

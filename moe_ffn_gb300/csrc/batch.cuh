@@ -50,7 +50,7 @@ struct BatchParams {
     float* topk_w_out;
     const float* norm_w;    // null, or the ffn_norm weight [H]
     float eps;
-    unsigned* err;
+    DevCtl* err;
 };
 
 struct BatchLayout {
@@ -96,22 +96,16 @@ __host__ __device__ inline BatchLayout batch_layout(const BatchParams& b) {
     return L;
 }
 
-// An order-preserving key of a float: larger floats, larger keys; -0 ranks
-// with +0.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    uint32_t b = __float_as_uint(v);
-    if ((b << 1) == 0u) b = 0u;
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
 // Routing of one token by one warp: softmax over the E logits, the k
 // largest (ties: lower expert index), renormalised over those k — as
-// route_topk, with the same weights: w_s = exp(l_s - l_0) / sum over the k
+// route_topk, with the same ranking keys (route.cuh), the same non-finite
+// rule and the same weights: w_s = exp(l_s - l_0) / sum over the k
 // selected (over all E with renorm = 0).  Lane l holds experts
 // [l*m, l*m + m), so among equal keys the lowest lane holds the lowest
-// index; k rounds of a warp max pick the ranks in order.
+// index; k rounds of a warp max pick the ranks in order.  A taken expert's
+// key becomes 0, which no logit has.
 __device__ __forceinline__ void route_warp(const float* __restrict__ lg, int E, int k, int lane,
-                                           int renorm, int32_t* idx, float* w) {
+                                           int renorm, int32_t* idx, float* w, DevCtl* err) {
     constexpr int M = MAX_EXPERTS / 32;
     const int m = (E + 31) >> 5;
     uint32_t key[M];
@@ -121,20 +115,18 @@ __device__ __forceinline__ void route_warp(const float* __restrict__ lg, int E, 
         const int e = lane * m + j;
         const bool valid = j < m && e < E;
         val[j] = valid ? __ldcg(lg + e) : 0.f;
-        key[j] = valid ? order_key(val[j]) : 0u;
+        key[j] = valid ? route_key(val[j]) : 0u;
     }
     int my_e = 0;
-    float my_l = 0.f;
+    uint32_t my_key = 0u;
     for (int s = 0; s < k; ++s) {
         uint32_t bk = 0u;
         int bj = 0;
-        float bl = 0.f;
 #pragma unroll
         for (int j = 0; j < M; ++j)
             if (key[j] > bk) {
                 bk = key[j];
                 bj = j;
-                bl = val[j];
             }
         const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
         const int wl = __ffs(__ballot_sync(0xffffffffu, bk == mx)) - 1;
@@ -144,12 +136,14 @@ __device__ __forceinline__ void route_warp(const float* __restrict__ lg, int E, 
                 if (j == bj) key[j] = 0u;
         }
         const int e = __shfl_sync(0xffffffffu, lane * m + bj, wl);
-        const float l = __shfl_sync(0xffffffffu, bl, wl);
         if (lane == s) {
             my_e = e;
-            my_l = l;
+            my_key = mx;
         }
     }
+    bool bad = false;
+    if (lane < k) my_e = route_clamp(my_e, E, &bad);
+    const float my_l = route_key_value(my_key);
     const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
     const float pr = lane < k ? expf(my_l - lmax) : 0.f;
     float z = pr;
@@ -161,10 +155,16 @@ __device__ __forceinline__ void route_warp(const float* __restrict__ lg, int E, 
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    float wv = pr / z;
+    if (route_degenerate(lmax)) {
+        my_e = lane;
+        wv = __int_as_float(0x7FC00000);
+    }
     if (lane < k) {
         idx[lane] = my_e;
-        w[lane] = pr / z;
+        w[lane] = wv;
     }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(err, DEV_ROUTE_RANGE);
 }
 
 // Pair lists shared by the consumer phases (shared memory).
@@ -381,6 +381,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     pdl_wait();
     pdl_trigger();
     if (tid == 0 && !sync_open(b.sync, b.err)) s_abort = 1;
+    const bool arrive = tid == 0 && arrives(b.err);
     const int H4 = H / 4;
     const float4* x4 = reinterpret_cast<const float4*>(b.x);
     if (b.norm_w) {
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
         }
     }
     named_bar(1, NC);
-    if (tid == 0 && !s_abort && !grid_barrier(b.sync, 1, b.err)) s_abort = 1;
+    if (tid == 0 && !s_abort && !grid_barrier(b.sync, 1, b.err, arrive)) s_abort = 1;
     named_bar(1, NC);
     if (s_abort) {
         if (tid == 0) sync_invalidate(b.sync);
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     // routing: one warp per token
     for (int t = warp; t < T; t += NCW)
         route_warp(b.logits + static_cast<int64_t>(t) * E, E, K, lane, b.gu.renorm,
-                   s_ridx + t * K, s_rw + t * K);
+                   s_ridx + t * K, s_rw + t * K, b.err);
     for (int e = tid; e < E; e += NC) s_mask[e] = 0u;
     named_bar(1, NC);
     if (cta == 0) {
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
                                            te * 16, it, tid);
     // every CTA's activations must be complete before any CTA reads them
     named_bar(1, NC);
-    if (tid == 0 && good && !grid_barrier(b.sync, 2u, b.err)) s_abort = 1;
+    if (tid == 0 && good && !grid_barrier(b.sync, 2u, b.err, arrive)) s_abort = 1;
     named_bar(1, NC);
     if (!good || s_abort) {
         if (tid == 0) sync_invalidate(b.sync);

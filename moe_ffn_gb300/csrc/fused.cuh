@@ -24,8 +24,8 @@
 // Grid barriers count arrivals in the first bytes of the workspace, which
 // the kernel validates and resets itself (sync_open / sync_close below), so
 // the workspace may hold anything.
-// Every wait is bounded (~2 s); on expiry the kernel records an error code
-// and returns.
+// Every wait is bounded (2 s unless a test shortened the limit); on expiry
+// the kernel records an error code and returns.
 #pragma once
 #include "stream.cuh"
 
@@ -43,7 +43,7 @@ struct FusedParams {
     float* topk_w_out;        // nullable
     const float* norm_w;      // nullable: ffn_norm weight [H]; gu.x is then the hidden state
     float eps;
-    unsigned* err;
+    DevCtl* err;
 };
 
 struct FusedLayout {
@@ -98,7 +98,7 @@ __device__ __forceinline__ void sync_invalidate(unsigned long long* sync) {
 }
 
 // By one thread per CTA, after the dependency wait.  False on a timeout.
-__device__ __forceinline__ bool sync_open(unsigned long long* sync, unsigned* err) {
+__device__ __forceinline__ bool sync_open(unsigned long long* sync, DevCtl* err) {
     if (ld_acquire_u64(sync + SYNC_TAG) == SYNC_VALID) return true;
     if (blockIdx.x == 0) {
         sync[SYNC_ARRIVE] = 0;
@@ -107,9 +107,10 @@ __device__ __forceinline__ bool sync_open(unsigned long long* sync, unsigned* er
         return true;
     }
     const uint64_t t0 = global_ns();
+    const unsigned long long lim = wait_limit(err);
     while (ld_acquire_u64(sync + SYNC_TAG) != SYNC_VALID) {
-        if (global_ns() - t0 > 2000000000ull) {
-            atomicCAS(err, 0u, DEV_TIMEOUT_GRID);
+        if (global_ns() - t0 > lim) {
+            record_error(err, DEV_TIMEOUT_GRID);
             return false;
         }
         __nanosleep(64);
@@ -117,18 +118,28 @@ __device__ __forceinline__ bool sync_open(unsigned long long* sync, unsigned* er
     return true;
 }
 
+// Whether this CTA arrives at the grid barriers (by one thread per CTA at the
+// kernel's start): always, unless a fault-injection test named it.
+__device__ __forceinline__ bool arrives(const DevCtl* err) {
+    return __ldcg(&err->skip_arrive_cta) != static_cast<int>(blockIdx.x);
+}
+
 // Grid barrier number `n` (1, 2, ...) of this call, by one thread per CTA
 // after a CTA barrier has ordered the CTA's writes.  The arrival is a
 // release, the wait an acquire (no full fence: one would also wait for the
 // producer's copies in flight).  False if the other CTAs did not arrive
-// within ~2 s.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* sync, unsigned n, unsigned* err) {
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(sync + SYNC_ARRIVE) : "memory");
+// within the wait limit.  `arrive` is false only in a fault-injection test.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* sync, unsigned n, DevCtl* err,
+                                             bool arrive = true) {
+    if (arrive)
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(sync + SYNC_ARRIVE)
+                     : "memory");
     const unsigned long long target = static_cast<unsigned long long>(n) * gridDim.x;
     const uint64_t t0 = global_ns();
+    const unsigned long long lim = wait_limit(err);
     while (ld_acquire_u64(sync + SYNC_ARRIVE) < target) {
-        if (global_ns() - t0 > 2000000000ull) {
-            atomicCAS(err, 0u, DEV_TIMEOUT_GRID);
+        if (global_ns() - t0 > lim) {
+            record_error(err, DEV_TIMEOUT_GRID);
             sync_invalidate(sync);
             return false;
         }
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fused_ffn_kernel(const FusedParam
     ring.stage_bytes = f.gu.stage_bytes;
     int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.off_tidx);
     float* s_w = reinterpret_cast<float*>(smem + L.off_tw);
-    float* s_logit = reinterpret_cast<float*>(smem + L.off_logit);
+    uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + L.off_logit);
     float* red = reinterpret_cast<float*>(smem + L.off_red);
     float* rpart = reinterpret_cast<float*>(smem + L.off_rpart);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
@@ -208,6 +219,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fused_ffn_kernel(const FusedParam
     pdl_wait();
     pdl_trigger();
     if (tid == 0 && !sync_open(f.sync, f.err)) s_abort = 1;
+    const bool arrive = tid == 0 && arrives(f.err);
     // ffn_norm (optional): every CTA reads the whole hidden state anyway
     const float inv =
         f.norm_w ? rms_inverse(f.gu.x, f.gu.nb_seg * 256, f.eps, red, tid, NC, 1) : 1.f;
@@ -257,14 +269,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) fused_ffn_kernel(const FusedParam
             named_bar(1, NC);
         }
         named_bar(1, NC);
-        if (tid == 0 && !s_abort && !grid_barrier(f.sync, 1, f.err)) s_abort = 1;
+        if (tid == 0 && !s_abort && !grid_barrier(f.sync, 1, f.err, arrive)) s_abort = 1;
         named_bar(1, NC);
         if (s_abort) {
             if (tid == 0) sync_invalidate(f.sync);
             named_bar_arrive(2, NTHREADS);  // release the producer, which then returns
             return;
         }
-        route_topk(f.logits, f.E, f.topk, s_logit, s_idx, s_w, tid, NC, 1, f.gu.renorm);
+        route_topk(f.logits, f.E, f.topk, s_key, s_idx, s_w, tid, NC, 1, f.gu.renorm, f.err);
         if (cta == 0 && tid < f.topk) {
             if (f.topk_idx_out) f.topk_idx_out[tid] = s_idx[tid];
             if (f.topk_w_out) f.topk_w_out[tid] = s_w[tid];
@@ -283,7 +295,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fused_ffn_kernel(const FusedParam
         consume_phase<FmtG, MODE_GATEUP>(f.gu, ring, s_idx, s_w, xq, xs, part, gb, ge, it, tid);
     // every CTA's activations a must be complete before any CTA reads them
     named_bar(1, NC);
-    if (tid == 0 && good && !grid_barrier(f.sync, f.moe ? 2u : 1u, f.err)) s_abort = 1;
+    if (tid == 0 && good && !grid_barrier(f.sync, f.moe ? 2u : 1u, f.err, arrive)) s_abort = 1;
     named_bar(1, NC);
     if (!good || s_abort) {
         if (tid == 0) sync_invalidate(f.sync);

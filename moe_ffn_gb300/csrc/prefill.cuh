@@ -27,6 +27,7 @@
 
 #include "formats.cuh"
 #include "ptx.cuh"
+#include "route.cuh"
 #include "umma.cuh"
 
 namespace qmoe {
@@ -97,47 +98,50 @@ __global__ void __launch_bounds__(256) pf_router_kernel(const float* __restrict_
 
 // ------------------------------------------------------------------ top-k
 // One warp per token.  Routing as the decode path (softmax over E, the k
-// largest with ties to the lower index, renormalised unless renorm = 0); each (token, slot)
+// largest with ties to the lower index, renormalised unless renorm = 0; the
+// ranking keys and the non-finite rule of route.cuh); each (token, slot)
 // pair is appended to its expert's list.  x is copied to f16 scaled by
 // 2^s_t, s_t chosen so that max |x| * 2^s_t lies in [2^14, 2^15).
 __global__ void __launch_bounds__(256) pf_topk_kernel(
     const float* __restrict__ logits, const float* __restrict__ X, int T, int H, int E, int K,
     int renorm, int32_t* __restrict__ tidx, float* __restrict__ tw, int32_t* __restrict__ user_idx,
     float* __restrict__ user_w, int32_t* __restrict__ cnt, int32_t* __restrict__ list,
-    __half* __restrict__ X16, float* __restrict__ xinv) {
+    __half* __restrict__ X16, float* __restrict__ xinv, DevCtl* err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     pdl_wait();
     pdl_trigger();
     if (t >= T) return;
-    // logits of this token: lane holds experts lane, lane+32, ... (E <= 256)
+    // logits of this token: lane holds experts lane, lane+32, ... (E <= 256),
+    // ranked on the total-order keys of route.cuh (ties: lower index), so
+    // the ranks are a permutation and every one of the K slots is written
     float lv[8];
+    uint32_t kv[8];
     const float* lt = logits + static_cast<int64_t>(t) * E;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
         lv[i] = e < E ? __ldcg(lt + e) : -INFINITY;
+        kv[i] = e < E ? route_key(lv[i]) : 0u;
     }
-    // rank of each of the lane's logits against all E
     int rank[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) rank[i] = 0;
     for (int j = 0; j < 8; ++j) {
         if (32 * j >= E) break;
         for (int src = 0; src < 32; ++src) {
-            const float w = __shfl_sync(0xffffffffu, lv[j], src);
+            const uint32_t w = __shfl_sync(0xffffffffu, kv[j], src);
             const int u = 32 * j + src;
             if (u >= E) continue;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane + 32 * i;
-                rank[i] += (w > lv[i]) || (w == lv[i] && u < e);
-            }
+            for (int i = 0; i < 8; ++i) rank[i] += route_before(w, u, kv[i], lane + 32 * i);
         }
     }
     // the selected experts, by rank: lane holding rank r publishes it
     __shared__ int32_t s_idx[8][16];
     __shared__ float s_l[8][16];
+    if (lane < K) s_idx[warp][lane] = -1;
+    __syncwarp();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
@@ -159,6 +163,8 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(
     }
     if (lane == 0) {
         const float lmax = s_l[warp][0];
+        const bool degen = route_degenerate(lmax);  // route 0..K-1, NaN weights
+        bool bad = false;
         float p[16], z = 0.f;
         for (int s = 0; s < K; ++s) {
             p[s] = expf(s_l[warp][s] - lmax);
@@ -166,8 +172,12 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(
         }
         const float inv = 1.0f / (renorm ? z : zall);
         for (int s = 0; s < K; ++s) {
-            const int e = s_idx[warp][s];
-            const float w = p[s] * inv;
+            int e = route_clamp(s_idx[warp][s], E, &bad);
+            float w = p[s] * inv;
+            if (degen) {
+                e = s;
+                w = __int_as_float(0x7FC00000);
+            }
             const int64_t pair = static_cast<int64_t>(t) * K + s;
             tidx[pair] = e;
             tw[pair] = w;
@@ -176,6 +186,7 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(
             const int pos = atomicAdd(&cnt[e], 1);
             list[static_cast<int64_t>(e) * T + pos] = static_cast<int32_t>(pair);
         }
+        if (bad) record_error(err, DEV_ROUTE_RANGE);
     }
     // x -> f16 with a power-of-two scale
     const float4* x4 = reinterpret_cast<const float4*>(X + static_cast<int64_t>(t) * H);
@@ -213,7 +224,7 @@ struct PfParams {
     const float* tw;
     float* a;         // [T*K][F] activations
     float* residual;  // [T][H]
-    unsigned* err;
+    DevCtl* err;
 };
 
 constexpr int PF_NP = 128;                // max tokens per pass (TMEM columns per region)
@@ -453,7 +464,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     // largest |value| of either half: 15|d*sc| + |dmin*m|
                     const float bound = fmaxf(fmaf(15.f, fabsf(d1), fabsf(m1)),
                                               fmaf(15.f, fabsf(d2), fabsf(m2)));
-                    if (bound > 65504.f && bound < INFINITY) atomicCAS(p.err, 0u, DEV_PF_RANGE);
+                    if (bound > 65504.f && bound < INFINITY) record_error(p.err, DEV_PF_RANGE);
                     const float A1 = 256.f * d1, C1 = -fmaf(128.f, d1, m1);
                     const float A2 = 256.f * d2, C2 = -fmaf(128.f, d2, m2);
                     const uint4 q0 = *reinterpret_cast<const uint4*>(sb + 16 + 32 * qtr);

@@ -6,9 +6,28 @@
 
 namespace qmoe {
 
-// Device-wide error word: set (first error wins) when a bounded wait runs out;
-// read and cleared by qmoe_device_status().
-enum : unsigned { DEV_OK = 0, DEV_TIMEOUT_FULL = 1, DEV_TIMEOUT_EMPTY = 2 };
+// Device error codes: the first one recorded wins; read and cleared by
+// qmoe_device_status().
+enum : unsigned { DEV_OK = 0, DEV_TIMEOUT_FULL = 1, DEV_TIMEOUT_EMPTY = 2, DEV_ROUTE_RANGE = 5 };
+
+// The device control block, one per device (a global of the library): the
+// error word, the limit of every bounded wait, and a fault-injection setting
+// for tests (a CTA that never arrives at the grid barriers, so that the
+// other CTAs' bounded waits run out).  The host sets the last two only
+// through qmoe_set_fault_injection; by default waits give up after 2 s.
+struct DevCtl {
+    unsigned code;                // 0, or the first error code recorded
+    int skip_arrive_cta;          // -1: none
+    unsigned long long wait_ns;   // limit of a bounded wait, nanoseconds
+};
+constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
+
+__device__ __forceinline__ void record_error(DevCtl* c, unsigned code) {
+    atomicCAS(&c->code, 0u, code);
+}
+__device__ __forceinline__ unsigned long long wait_limit(const DevCtl* c) {
+    return __ldcg(&c->wait_ns);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -56,15 +75,17 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Bounded wait on a barrier phase.  Returns false (and records `code` in the
-// device error word) if the phase has not completed within ~2 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  unsigned* err, unsigned code) {
+// device error word) if the phase has not completed within the wait limit
+// (2 s unless a test shortened it).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, DevCtl* err,
+                                                  unsigned code) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
+    const unsigned long long lim = wait_limit(err);
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_ns() - t0 > 2000000000ull) {
-            atomicCAS(err, 0u, code);
+        if ((i & 255u) == 0 && global_ns() - t0 > lim) {
+            record_error(err, code);
             return false;
         }
     }

@@ -5,10 +5,12 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdarg>
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -39,8 +41,9 @@ static qmoe_status cuda_fail(cudaError_t e, const char* what) {
     return fail(QMOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Device error word (bounded waits record here).
-__device__ unsigned g_dev_err;
+// The device control block (ptx.cuh): error word, wait limit, fault
+// injection.  One per device that loads the library.
+__device__ DevCtl g_dev_ctl = {0u, -1, DEFAULT_WAIT_NS};
 
 // ------------------------------------------------------------ formats
 static int block_elems(int qt) {
@@ -91,7 +94,7 @@ struct DevInfo {
     bool supported = false;
     int sms = 0;
     int smem_optin = 0;
-    unsigned* err = nullptr;
+    DevCtl* err = nullptr;
     int cc_major = 0, cc_minor = 0;
 };
 static DevInfo g_dev[64];
@@ -115,9 +118,9 @@ static qmoe_status device_info(DevInfo** out) {
         d.supported = (prop.major == 10 && prop.minor == 3);
         if (d.supported) {
             void* p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_dev_err);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
-            d.err = static_cast<unsigned*>(p);
+            e = cudaGetSymbolAddress(&p, g_dev_ctl);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device control)");
+            d.err = static_cast<DevCtl*>(p);
         }
         d.init = true;
     }
@@ -306,26 +309,16 @@ static int dispatch_fused_d(int dq, const FusedParams& f, const DevInfo& d, cuda
     }
 }
 
-// Fused layer for these formats: 1 launched, 0 not applicable (the caller
-// runs separate kernels), negative on a CUDA error.  The fused kernel can be
-// switched off with the environment variable QMOE_FUSED=0 (diagnostics).
-static bool fused_enabled() {
-    static const bool on = [] {
-        const char* e = getenv("QMOE_FUSED");
-        return !(e && e[0] == '0');
-    }();
-    return on;
-}
+// Execution mode (qmoe_set_exec_mode; diagnostics and tests): the default
+// kernels, or the separate-kernel forms they replace.
+static std::atomic<int> g_exec_mode{QMOE_EXEC_DEFAULT};
 
-// The batched decode kernel for 2..31 tokens (QMOE_BATCH=0 runs those
-// tokens one fused launch at a time instead, for diagnostics).
-static bool batch_enabled() {
-    static const bool on = [] {
-        const char* e = getenv("QMOE_BATCH");
-        return fused_enabled() && !(e && e[0] == '0');
-    }();
-    return on;
-}
+// Fused layer for these formats: 1 launched, 0 not applicable (the caller
+// runs separate kernels), negative on a CUDA error.
+static bool fused_enabled() { return g_exec_mode.load() != QMOE_EXEC_SEPARATE; }
+
+// The batched decode kernel for 2..31 tokens.
+static bool batch_enabled() { return g_exec_mode.load() == QMOE_EXEC_DEFAULT; }
 
 static int dispatch_fused(int gq, int dq, const FusedParams& f, const DevInfo& d, cudaStream_t st,
                           qmoe_status* err) {
@@ -736,7 +729,7 @@ static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
     const int renorm = (s.route_flags & QMOE_ROUTE_NO_RENORM) ? 0 : 1;
     e = launch_pdl(pf::pf_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st,
                    static_cast<const float*>(logits), x, T, H, E, K, renorm, tidx, tw, topk_idx,
-                   topk_w, cnt, list, x16, xinv);
+                   topk_w, cnt, list, x16, xinv, d.err);
     if (e != cudaSuccess) return cuda_fail(e, "pf_topk launch");
 
     static int configured[64] = {};
@@ -1049,10 +1042,12 @@ qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const
                     "moe_ffn_noalloc: this shape needs %zu bytes of scratch; the built-in "
                     "scratch holds %zu (use moe_ffn with a workspace)",
                     need, static_cast<size_t>(QMOE_NOALLOC_SCRATCH_BYTES));
+    // the device must be one this library runs on before its scratch is looked up
+    DevInfo* d = nullptr;
+    if (qmoe_status r = device_info(&d)) return r;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return fail(QMOE_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
     void* ws = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -1068,6 +1063,36 @@ qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const
                    topk_w, ws, QMOE_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+qmoe_status qmoe_set_exec_mode(int mode) {
+    g_last_error.clear();
+    if (mode != QMOE_EXEC_DEFAULT && mode != QMOE_EXEC_SEPARATE && mode != QMOE_EXEC_UNBATCHED)
+        return fail(QMOE_ERR_INVALID_ARGUMENT, "qmoe_set_exec_mode: unknown mode %d", mode);
+    g_exec_mode.store(mode);
+    return QMOE_OK;
+}
+
+qmoe_status qmoe_set_fault_injection(uint64_t wait_limit_ns, int skip_arrive_cta) {
+    g_last_error.clear();
+    DevInfo* d = nullptr;
+    if (qmoe_status s = device_info(&d)) return s;
+    if (skip_arrive_cta < -1)
+        return fail(QMOE_ERR_INVALID_ARGUMENT,
+                    "qmoe_set_fault_injection: skip_arrive_cta=%d must be >= -1", skip_arrive_cta);
+    DevCtl c;
+    c.code = 0u;
+    c.skip_arrive_cta = skip_arrive_cta;
+    c.wait_ns = wait_limit_ns ? static_cast<unsigned long long>(wait_limit_ns) : DEFAULT_WAIT_NS;
+    // everything after the error word; the device is idle first, so no
+    // kernel sees a half-written setting
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = cudaMemcpy(reinterpret_cast<uint8_t*>(d->err) + offsetof(DevCtl, skip_arrive_cta),
+                   &c.skip_arrive_cta, sizeof(DevCtl) - offsetof(DevCtl, skip_arrive_cta),
+                   cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "write device control");
+    return QMOE_OK;
+}
+
 qmoe_status qmoe_device_status(void* stream) {
     g_last_error.clear();
     DevInfo* d = nullptr;
@@ -1075,15 +1100,19 @@ qmoe_status qmoe_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     unsigned v = 0, zero = 0;
-    e = cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(&v, &d->err->code, sizeof v, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "read device error word");
     if (v) {
-        e = cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        e = cudaMemcpy(&d->err->code, &zero, sizeof zero, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
         if (v == pf::DEV_PF_RANGE)
             return fail(QMOE_ERR_UNSUPPORTED,
                         "a decoded gate/up weight is outside f16 range (code %u); the "
                         "many-token path cannot represent it", v);
+        if (v == DEV_ROUTE_RANGE)
+            return fail(QMOE_ERR_CUDA,
+                        "internal error: the routing produced an expert index outside [0, E) "
+                        "(code %u); it was clamped, and the layer's output is not valid", v);
         return fail(QMOE_ERR_TIMEOUT, "a bounded device wait expired (code %u: %s)", v,
                     v == DEV_TIMEOUT_FULL    ? "stage never filled"
                     : v == DEV_TIMEOUT_EMPTY ? "stage never released"

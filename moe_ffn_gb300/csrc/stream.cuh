@@ -30,6 +30,7 @@
 #pragma once
 #include "formats.cuh"
 #include "ptx.cuh"
+#include "route.cuh"
 
 namespace qmoe {
 
@@ -70,7 +71,7 @@ struct StreamParams {
     int32_t* topk_idx_out;  // nullable, written by CTA 0 of GATEUP
     float* topk_w_out;
     int moe;
-    unsigned* err;
+    DevCtl* err;
 };
 
 template <int MODE> struct ModeGeom {
@@ -121,7 +122,10 @@ __host__ __device__ inline SmemLayout smem_layout(const StreamParams& p) {
 // moe_layer).  The renormalised weight of a selected expert equals
 // exp(l_s - l_max) / sum over the selected k of exp(l_t - l_max); with
 // renorm = 0 the sum runs over all E experts instead (the softmax
-// probability itself).
+// probability itself).  Experts are ranked on the total order of
+// route.cuh, so every one of the k slots is written whatever the logits
+// hold; when the top logit is not finite the route is experts 0..k-1 with
+// NaN weights (route.cuh).
 // Threads [0, nthr) of the CTA call it together; they synchronise on named
 // barrier `bar` (0: the whole CTA, nthr == blockDim.x).  k <= 32.
 __device__ __forceinline__ void group_sync(int bar, int nthr) {
@@ -131,51 +135,60 @@ __device__ __forceinline__ void group_sync(int bar, int nthr) {
         named_bar(bar, nthr);
 }
 
-__device__ inline void route_topk(const float* __restrict__ logits, int E, int k, float* s_logit,
+__device__ inline void route_topk(const float* __restrict__ logits, int E, int k, uint32_t* s_key,
                                   int32_t* s_idx, float* s_w, int tid, int nthr, int bar,
-                                  int renorm) {
-    for (int e = tid; e < E; e += nthr) s_logit[e] = __ldcg(logits + e);
+                                  int renorm, DevCtl* err) {
+    for (int e = tid; e < E; e += nthr) s_key[e] = route_key(__ldcg(logits + e));
+    if (tid < k) s_idx[tid] = -1;
     group_sync(bar, nthr);
-    // two threads per expert: each counts the experts that beat it over half of E
+    // two threads per expert: each counts the experts ranked before it over half of E
     for (int base = 0; base < E; base += nthr / 2) {
         const int e = base + tid / 2, half = tid & 1;
         int rank = 0;
         if (e < E) {
-            const float v = s_logit[e];
+            const uint32_t v = s_key[e];
             const int u0 = half ? E / 2 : 0, u1 = half ? E : E / 2;
             int u = u0;
-            if ((E & 7) == 0) {  // both halves are whole float4s
-                const float4* l4 = reinterpret_cast<const float4*>(s_logit);
+            if ((E & 7) == 0) {  // both halves are whole uint4s
+                const uint4* k4 = reinterpret_cast<const uint4*>(s_key);
 #pragma unroll 4
                 for (; u < u1; u += 4) {
-                    const float4 w = l4[u >> 2];
-                    rank += (w.x > v) || (w.x == v && u < e);
-                    rank += (w.y > v) || (w.y == v && u + 1 < e);
-                    rank += (w.z > v) || (w.z == v && u + 2 < e);
-                    rank += (w.w > v) || (w.w == v && u + 3 < e);
+                    const uint4 w = k4[u >> 2];
+                    rank += route_before(w.x, u, v, e);
+                    rank += route_before(w.y, u + 1, v, e);
+                    rank += route_before(w.z, u + 2, v, e);
+                    rank += route_before(w.w, u + 3, v, e);
                 }
             }
-            for (; u < u1; ++u) {
-                const float w = s_logit[u];
-                rank += (w > v) || (w == v && u < e);
-            }
+            for (; u < u1; ++u) rank += route_before(s_key[u], u, v, e);
         }
         rank += __shfl_xor_sync(0xffffffffu, rank, 1);
         if (e < E && half == 0 && rank < k) s_idx[rank] = e;
     }
     group_sync(bar, nthr);
     if (tid < 32) {
-        const float l = tid < k ? s_logit[s_idx[tid]] : 0.f;
+        bool bad = false;
+        int e = tid < k ? route_clamp(s_idx[tid], E, &bad) : 0;
+        const float l = tid < k ? route_key_value(s_key[e]) : 0.f;
         const float lmax = __shfl_sync(0xffffffffu, l, 0);
         const float pr = tid < k ? expf(l - lmax) : 0.f;
         float z = pr;
         if (!renorm) {
             z = 0.f;
-            for (int e = tid; e < E; e += 32) z += expf(s_logit[e] - lmax);
+            for (int u = tid; u < E; u += 32) z += expf(route_key_value(s_key[u]) - lmax);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        if (tid < k) s_w[tid] = pr / z;
+        float w = pr / z;
+        if (route_degenerate(lmax)) {
+            e = tid;
+            w = __int_as_float(0x7FC00000);
+        }
+        if (tid < k) {
+            s_idx[tid] = e;
+            s_w[tid] = w;
+        }
+        if (__any_sync(0xffffffffu, bad) && tid == 0) record_error(err, DEV_ROUTE_RANGE);
     }
     group_sync(bar, nthr);
 }
@@ -500,8 +513,19 @@ __device__ __forceinline__ uint32_t chunk_copy(const StreamParams& p, const int3
         ((sa + static_cast<uintptr_t>(cd.nbp) * Fmt::SBB + 15) & ~uintptr_t(15)) - src);
 }
 
+// After a wait of the producer gave up: wait (bounded) until the copies of
+// the last chunks it issued, numbers [it - nstages, it), have landed, so the
+// CTA never exits with a bulk copy still writing its shared memory.
+__device__ inline void ring_drain(const Ring& ring, int it, DevCtl* err) {
+    for (int j = it - ring.nstages; j < it; ++j)
+        if (j >= 0)
+            mbar_wait_bounded(&ring.full[j % ring.nstages], (j / ring.nstages) & 1, err,
+                              DEV_TIMEOUT_FULL);
+}
+
 // Producer warp: stream every chunk of the units [ubeg, uend) into the ring.
-// False if a wait for a free stage timed out (the error word is set).
+// False if a wait for a free stage timed out (the error word is set; the
+// copies already issued have landed).
 template <class Fmt, int MODE>
 __device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int32_t* s_idx,
                               int64_t ubeg, int64_t uend, int& it, int lane) {
@@ -515,8 +539,10 @@ __device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int
             const int s = it % ring.nstages;
             const int round = it / ring.nstages;
             if (round > 0 &&
-                !mbar_wait_bounded(&ring.empty[s], (round - 1) & 1, p.err, DEV_TIMEOUT_EMPTY))
+                !mbar_wait_bounded(&ring.empty[s], (round - 1) & 1, p.err, DEV_TIMEOUT_EMPTY)) {
+                ring_drain(ring, it, p.err);
                 return false;
+            }
             const ChunkDesc cd = chunk_desc(p, c);
             const int ncopy = chunk_copies<MODE>(p, cd);
             uint32_t mine = 0;
@@ -688,7 +714,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
     ring.stage_bytes = p.stage_bytes;
     int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.off_tidx);
     float* s_w = reinterpret_cast<float*>(smem + L.off_tw);
-    float* s_logit = reinterpret_cast<float*>(smem + L.off_logit);
+    uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + L.off_logit);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
     uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.off_xq);
@@ -714,11 +740,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
     // this grid was allowed to start; the gate/up kernel reads them right
     // after its own dependency wait.
     if (p.moe && MODE == MODE_DOWN) {
-        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0, p.renorm);
+        route_topk(p.logits, p.E, p.topk, s_key, s_idx, s_w, tid, NTHREADS, 0, p.renorm, p.err);
     } else if (p.moe && MODE == MODE_GATEUP) {
         pdl_wait();
         pdl_trigger();
-        route_topk(p.logits, p.E, p.topk, s_logit, s_idx, s_w, tid, NTHREADS, 0, p.renorm);
+        route_topk(p.logits, p.E, p.topk, s_key, s_idx, s_w, tid, NTHREADS, 0, p.renorm, p.err);
         if (blockIdx.x == 0 && tid < p.topk) {
             if (p.topk_idx_out) p.topk_idx_out[tid] = s_idx[tid];
             if (p.topk_w_out) p.topk_w_out[tid] = s_w[tid];

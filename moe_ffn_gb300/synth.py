@@ -80,7 +80,8 @@ def normal(g: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- workloads
-# Sizes of the five workloads (see the design doc for the full recipe).
+# Sizes of the five workloads; the value distributions are those of the
+# generators above.
 GEMV_SMALL = dict(qtype=Q4_0, rows=256, cols=1024)                       # single Q4_0 matvec
 GEMV_SWEEP = dict(qtypes=(Q8_0, Q4_0, Q4_K, Q5_K, Q6_K), rows=4096, cols=4096, nan_row=1)
 DENSE_FFN = dict(hidden=4096, inter=14336, gate=Q4_K, up=Q4_K, down=Q6_K)

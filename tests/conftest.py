@@ -34,4 +34,9 @@ def qm():
     import moe_ffn_gb300 as qm
     qm.build()
     qm.lib()
+    # child test processes of test_gpu_unfused.py run the suite in one of the
+    # library's other kernel forms
+    mode = os.environ.get("QMOE_TEST_EXEC_MODE")
+    if mode:
+        qm.set_exec_mode(int(mode))
     return qm

@@ -156,3 +156,17 @@ def test_rmsnorm_refusals(lib):
     assert ffn(eps=-0.5) == qm.ERR_INVALID_ARGUMENT
     assert ffn(ws_bytes=qm.ffn_swiglu_workspace_size(4096, 14336)) == qm.ERR_INVALID_ARGUMENT
     assert "ffn_swiglu_rmsnorm" in qm.last_error()
+
+
+def test_noalloc_scratch_constant_matches_header():
+    """The binding's NOALLOC_SCRATCH_BYTES is the header's macro."""
+    text = open(qm.HEADER).read()
+    m = re.search(r"#define\s+QMOE_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "QMOE_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert int(m.group(1)) << int(m.group(2)) == qm.NOALLOC_SCRATCH_BYTES
+
+
+def test_exec_mode_refuses_unknown(lib):
+    assert lib.qmoe_set_exec_mode(7) == qm.ERR_INVALID_ARGUMENT
+    assert "mode" in qm.last_error()
+    assert lib.qmoe_set_exec_mode(qm.EXEC_DEFAULT) == qm.OK

@@ -297,3 +297,34 @@ def test_moe_many_tokens_f16_range_reported(qm):
     assert qm.device_status() == qm.ERR_UNSUPPORTED
     assert "f16 range" in qm.last_error()
     assert qm.device_status() == qm.OK
+
+
+# ------------------------------------------------- non-finite activations
+NON_FINITE = [
+    dict(synth.MOE_DECODE),                                                # fused, 1 token
+    dict(synth.MOE_DECODE, n_tokens=5),                                    # batched
+    dict(hidden=512, expert_dim=256, num_experts=16, top_k=4, n_tokens=64,
+         gate=synth.Q4_K, up=synth.Q4_K, down=synth.Q6_K),                 # tensor cores
+]
+
+
+@pytest.mark.parametrize("bad", ["nan", "inf"])
+@pytest.mark.parametrize("shp", NON_FINITE, ids=lambda s: "T{n_tokens}".format(**s))
+def test_moe_non_finite_activation(qm, orc, shp, bad):
+    """One activation of one token is NaN or +Inf.  That token's logits are
+    then NaN or +-Inf, its softmax is NaN throughout, and its route is experts
+    0..k-1 with NaN weights (the order the oracle's stable sort leaves NaN
+    probabilities in); its residual becomes NaN.  Every slot names an expert
+    in range, and the other tokens are routed and computed as usual."""
+    inp = synth.moe_inputs(61 + shp["n_tokens"], **shp)
+    T, K = shp["n_tokens"], shp["top_k"]
+    tb = T // 2
+    inp["x"] = inp["x"].copy()
+    inp["x"].reshape(T, -1)[tb, 100] = np.nan if bad == "nan" else np.inf
+    out, idx, w = gpu_moe(qm, inp, shp)
+    assert qm.device_status() == qm.OK
+    ref = oracle_moe(orc, inp, shp)
+    assert list(ref["idx"][tb]) == list(range(K)) and np.all(np.isnan(ref["w"][tb]))
+    assert idx[tb].tolist() == list(range(K))
+    assert np.all(np.isnan(w[tb])) and np.all(np.isnan(out.reshape(T, -1)[tb]))
+    assert check_moe(out, idx, w, ref) <= max(1, T // 20)
