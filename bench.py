@@ -174,7 +174,13 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    ms_local = time_replays(torch, g_sweep, replays)
+    # the K-step timed region, repeated; the median repetition is reported
+    regions = []
+    for _ in range(args.repeats):
+        barrier(world)
+        torch.cuda.synchronize()
+        regions.append(time_replays(torch, g_sweep, replays))
+    ms_local = statistics.median(regions)
     barrier(world)
     ms_total = max_over_ranks(ms_local, world, dev)
     ms_step = ms_total / steps_timed
@@ -193,7 +199,7 @@ def run_ours(args, rank, world):
         gf = capture(torch, one, L)
         gf.replay()
         torch.cuda.synchronize()
-        us = time_replays(torch, gf, 5) * 1e3 / (5 * L)
+        us = time_graph(torch, gf) * 1e3 / L
         alg = bytes_w[n] + 4 * COLS + 4 * ROWS
         per_fmt[n] = {"us": round(us, 3), "gbs": round(alg / us / 1e3, 1),
                       "frac": round(alg / us / 1e3 / peak, 3), "bytes": alg}
@@ -249,6 +255,9 @@ def run_ours(args, rank, world):
                    "rows": ROWS, "cols": COLS, "weight_copies": n_copies,
                    "l2": "weights rotate over copies totalling > 4x L2 (no flush needed)",
                    "launch": f"CUDA graph of {n_copies} steps, replayed",
+                   "timed_region": f"{steps_timed} steps, repeated {args.repeats} times; "
+                                   "the median repetition",
+                   "arithmetic": "GGUF blocks decoded exactly; f32 activations, f32 sums",
                    "parallelism": f"replicas{world}"},
         "roofline": {"bound": "hbm", "kernel": f"stream_gemv_kernel<{dom}, QMV>",
                      "achieved": per_fmt[dom]["gbs"], "peak": peak, "unit": "GB/s",
@@ -264,7 +273,8 @@ def run_ours(args, rank, world):
     }
     line.update(extra)
     if rank == 0 and world == 1 and not args.skip_cpu:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, all_cores=True)
+        line["cpu_baseline_1core"] = cpu_baseline(args.cpu_seconds)
     return line
 
 
@@ -298,6 +308,17 @@ def time_replays(torch, g, replays):
     return e0.elapsed_time(e1)
 
 
+def time_graph(torch, g, min_s=0.5, chunk_ms=25.0):
+    """Median ms per replay of graph g over a timed span of at least min_s:
+    chunks of about chunk_ms of back-to-back replays, each timed with CUDA
+    events; the median of the chunks' per-replay times."""
+    one = max(time_replays(torch, g, 2) / 2, 1e-3)
+    per_chunk = max(1, int(chunk_ms / one))
+    n_chunks = max(5, int(min_s * 1e3 / (per_chunk * one)) + 1)
+    return statistics.median(time_replays(torch, g, per_chunk) / per_chunk
+                             for _ in range(n_chunks))
+
+
 GEMV_SOURCES = ("formats.cuh", "ptx.cuh", "stream.cuh")
 
 
@@ -322,39 +343,38 @@ def load_traffic(key):
     return None
 
 
-def layer_launches(separate):
-    """Kernel launches per FFN layer / MoE token: one fused cooperative launch
-    (the bench never selects the separate-kernel form)."""
-    return 1
-
-
 def bench_layers(qm, synth, dev, stream, args):
     """MoE decode (us/token), dense FFN (us/call), MoE 512-token layer
     (us/token); each captured in a CUDA graph and replayed."""
     import torch
     out = {}
     peak, _ = load_peaks()
-    # MoE decode: full stacks resident (391.6 MB > L2); x rotates over 64
-    # token vectors so the routing (and the experts read) varies per call.
+    # MoE decode: NCOPY copies of the full stacks (391.6 MB each, 1.57 GB in
+    # all) rotate call by call, and x rotates over 64 token vectors, so the
+    # routing (and the experts read) varies per call and an expert's rows
+    # come back to the same copy only every NCOPY calls.
     shp = synth.MOE_DECODE
     inp = synth.moe_inputs(0, **shp)
     g = synth.rng(99)
     xpool = torch.from_numpy(synth.normal(g, (64, shp["hidden"]))).to(dev)
     s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], shp["top_k"], 1,
                      shp["gate"], shp["up"], shp["down"])
-    d = {k: torch.from_numpy(inp[k]).to(dev) for k in ("router", "gate", "up", "down")}
+    NCOPY = 4
+    dc = [{k: torch.from_numpy(inp[k]).to(dev) for k in ("router", "gate", "up", "down")}
+          for _ in range(NCOPY)]
+    d = dc[0]
     res = torch.from_numpy(inp["residual"]).to(dev)
     ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device=dev)
     idx = torch.empty((1, shp["top_k"]), dtype=torch.int32, device=dev)
 
     def call(i):
-        qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], s, xpool[i % 64], res, idx, None,
+        c = dc[i % NCOPY]
+        qm.moe_ffn(c["router"], c["gate"], c["up"], c["down"], s, xpool[i % 64], res, idx, None,
                    ws)
     n = 64
     gm = capture(torch, call, n)
     gm.replay()
-    reps = 4
-    us = time_replays(torch, gm, reps) * 1e3 / (reps * n)
+    us = time_graph(torch, gm) * 1e3 / n
     rb_g = qm.row_bytes(shp["gate"], shp["hidden"])
     rb_d = qm.row_bytes(shp["down"], shp["expert_dim"])
     alg = (shp["num_experts"] * shp["hidden"] * 4
@@ -362,8 +382,9 @@ def bench_layers(qm, synth, dev, stream, args):
            + 3 * shp["hidden"] * 4)
     out["moe_decode"] = {"us_per_token": round(us, 3), "alg_bytes": alg,
                          "gbs": round(alg / us / 1e3, 1), "frac": round(alg / us / 1e3 / peak, 3),
-                         "launches_per_token": layer_launches(3),
-                         "launch": f"CUDA graph of {n} tokens",
+                         "launches_per_token": 1,
+                         "launch": f"CUDA graph of {n} tokens over {NCOPY} stack copies "
+                                   f"(1.57 GB), replayed for >= 0.5 s, median",
                          "workload": "hidden 2048, 128 experts, top-8, expert_dim 768, Q4_K/Q4_K/Q6_K"}
     # the same layer with ffn_norm fused in front (input = the hidden state)
     nw = torch.from_numpy(synth.norm_weight(synth.rng(98), shp["hidden"])).to(dev)
@@ -371,11 +392,12 @@ def bench_layers(qm, synth, dev, stream, args):
     wsn = torch.zeros(qm.moe_ffn_rmsnorm_workspace_size(s), dtype=torch.uint8, device=dev)
 
     def ncall(i):
-        qm.moe_ffn_rmsnorm(d["router"], d["gate"], d["up"], d["down"], s, nw, 1e-6,
+        c = dc[i % NCOPY]
+        qm.moe_ffn_rmsnorm(c["router"], c["gate"], c["up"], c["down"], s, nw, 1e-6,
                            hpool[i % 64], idx, None, wsn)
     gn = capture(torch, ncall, n)
     gn.replay()
-    usn = time_replays(torch, gn, reps) * 1e3 / (reps * n)
+    usn = time_graph(torch, gn) * 1e3 / n
     out["moe_decode"]["us_per_token_with_ffn_norm"] = round(usn, 3)
     # small batches: T tokens per call, each routed expert read once per call
     xpool2 = torch.cat([xpool, xpool])
@@ -390,7 +412,8 @@ def bench_layers(qm, synth, dev, stream, args):
 
         def bcall(i, T=T, sT=sT, wsT=wsT, resT=resT, idxT=idxT):
             j = (i * T) % 64
-            qm.moe_ffn(d["router"], d["gate"], d["up"], d["down"], sT, xpool2[j:j + T], resT,
+            c = dc[i % NCOPY]
+            qm.moe_ffn(c["router"], c["gate"], c["up"], c["down"], sT, xpool2[j:j + T], resT,
                        idxT, None, wsT)
         nT = max(8, 64 // T)
         experts = []
@@ -399,7 +422,7 @@ def bench_layers(qm, synth, dev, stream, args):
             experts.append(len(np.unique(idxT.cpu().numpy())))
         gb = capture(torch, bcall, nT)
         gb.replay()
-        usb = time_replays(torch, gb, reps) * 1e3 / (reps * nT)
+        usb = time_graph(torch, gb) * 1e3 / nT
         ne = float(np.mean(experts))
         algb = shp["num_experts"] * shp["hidden"] * 4 + ne * per_expert + 3 * T * shp["hidden"] * 4
         batched[str(T)] = {"us_per_call": round(usb, 3), "us_per_token": round(usb / T, 3),
@@ -407,10 +430,10 @@ def bench_layers(qm, synth, dev, stream, args):
                            "frac": round(algb / usb / 1e3 / peak, 3)}
         del gb
     out["moe_decode"]["batched"] = batched
-    out["moe_decode"]["batched_launch"] = ("CUDA graph of max(8, 64/T) calls of T tokens; "
-                                           "alg bytes = router + distinct experts read + x, "
-                                           "residual in/out")
-    del d, inp, gm, gn
+    out["moe_decode"]["batched_launch"] = ("CUDA graph of max(8, 64/T) calls of T tokens over "
+                                           f"{NCOPY} stack copies, >= 0.5 s, median; alg bytes = "
+                                           "router + distinct experts read + x, residual in/out")
+    del d, dc, inp, gm, gn
     torch.cuda.empty_cache()
 
     # dense SwiGLU FFN: 114 MB weights, 5 copies rotating (> 4x L2)
@@ -432,11 +455,12 @@ def bench_layers(qm, synth, dev, stream, args):
     n = 2 * ncp
     gf = capture(torch, fcall, n)
     gf.replay()
-    us = time_replays(torch, gf, 4) * 1e3 / (4 * n)
+    us = time_graph(torch, gf) * 1e3 / n
     alg = fin["gate"].nbytes + fin["up"].nbytes + fin["down"].nbytes + 4 * w["hidden"] * 3
     out["dense_ffn"] = {"us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1),
-                        "frac": round(alg / us / 1e3 / peak, 3), "launches": layer_launches(2),
-                        "launch": f"CUDA graph of {n} calls",
+                        "frac": round(alg / us / 1e3 / peak, 3), "launches": 1,
+                        "launch": f"CUDA graph of {n} calls over {ncp} weight copies, "
+                                  ">= 0.5 s, median",
                         "workload": "hidden 4096, intermediate 14336, Q4_K/Q4_K/Q6_K"}
     del G, U, D, gf
     torch.cuda.empty_cache()
@@ -455,8 +479,7 @@ def bench_layers(qm, synth, dev, stream, args):
                    None, ws)
     gp = capture(torch, pcall, 1)
     gp.replay()
-    n = 3
-    us = time_replays(torch, gp, n) * 1e3 / n
+    us = time_graph(torch, gp) * 1e3
     rb_g = qm.row_bytes(shp["gate"], shp["hidden"])
     rb_d = qm.row_bytes(shp["down"], shp["expert_dim"])
     alg_w = shp["num_experts"] * (2 * shp["expert_dim"] * rb_g + shp["hidden"] * rb_d)
@@ -467,7 +490,7 @@ def bench_layers(qm, synth, dev, stream, args):
                           "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1),
                           "frac_hbm": round(alg / us / 1e3 / peak, 4),
                           "expert_tflops": round(flops / us / 1e6, 2),
-                          "launch": "CUDA graph of one call",
+                          "launch": "CUDA graph of one call, replayed for >= 0.5 s, median",
                           "workload": "512 tokens, hidden 2048, 64 experts, top-8, "
                                       "expert_dim 1024, Q4_K/Q4_K/Q6_K"}
     return out
@@ -487,11 +510,10 @@ def oracle_sweep_setup():
     return oracle, data
 
 
-def cpu_baseline(seconds=12.0, rows_sample=None):
-    """The oracle as it stands (plain C, one thread), timed on this host on
-    whole sweeps (all five 4096x4096 GEMVs) until `seconds` have passed."""
+def _oracle_sweeps(seconds):
+    """Whole sweeps (all five 4096x4096 GEMVs) of the oracle until `seconds`
+    have passed, in this process: (sweeps, elapsed seconds)."""
     orc, data = oracle_sweep_setup()
-    alg = sum(W.nbytes + 4 * COLS + 4 * ROWS for _, W, _ in data)
     t0 = time.perf_counter()
     n = 0
     while True:
@@ -500,10 +522,45 @@ def cpu_baseline(seconds=12.0, rows_sample=None):
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
-    return {"value": round(n * alg / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} full sweeps (5 x 4096x4096 GEMVs, decode-then-dot, fp64 "
-                      f"accumulation) in {dt:.1f} s"}
+    return n, time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            k, _, v = line.partition(":")
+            if k.strip() in ("model name", "Model name", "CPU part"):
+                return v.strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(seconds=12.0, all_cores=False):
+    """The oracle as it stands (plain C, one thread per process), timed on this
+    host on whole sweeps for about `seconds`: in this process, or (all_cores)
+    in one spawned process per host core at once, the bytes of every
+    process's sweeps over the wall time."""
+    alg = sum(W.nbytes + 4 * COLS + 4 * ROWS for _, W, _ in oracle_sweep_setup()[1])
+    if not all_cores:
+        n, dt = _oracle_sweeps(seconds)
+        return {"value": round(n * alg / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"{n} full sweeps (5 x 4096x4096 GEMVs, decode-then-dot, fp64 "
+                          f"accumulation) in {dt:.1f} s on one core of {cpu_model()}"}
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_sweeps, [seconds] * cores)
+    wall = time.perf_counter() - t0
+    n = sum(r[0] for r in res)
+    return {"value": round(n * alg / wall / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} full sweeps over {cores} processes (one oracle per core, "
+                      f"{seconds:.0f} s each) in {wall:.1f} s wall on {cpu_model()}"}
 
 
 def run_reference(args, rank, world):
@@ -608,7 +665,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-layers", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--repeats", type=int, default=50,
+                    help="repetitions of the K-step timed region (the median is reported)")
     ap.add_argument("--profile", default=None,
                     help="run one small case for ncu (gemv:<FMT>, moe, ffn) and exit")
     args = ap.parse_args(argv)

@@ -32,15 +32,20 @@
  *     blocks, row_bytes = cols / block_elems * block_bytes.  W must be 16-byte
  *     aligned; the kernels read whole 16-byte granules that contain W's bytes
  *     (never a byte outside those granules).
- *   - Floating-point results are f32.  The quantized products take the
- *     activations as 16-bit integers with one f32 scale per 32 elements (max |x|
- *     of the block / 32767) and sum quants times activations exactly in 32-bit
- *     integers per sub-block; scales, mins and everything after them are f32
- *     with FMA.  Results match the exact result within
- *     |err| <= 1e-3 * sum_j |w_ij x_j| + 1e-6 per GEMV output (the rounding of x
- *     adds at most sum_j |w_ij| * max |x| of j's block / 65534), NaN where the
- *     exact computation is NaN (a NaN scale or a NaN activation).  Non-finite
- *     inputs (Inf scales, non-finite x) give non-finite outputs, NaN or Inf.
+ *   - Floating-point arithmetic is f32, as the pages' kernels compute it:
+ *     every product of a decoded weight (an integer quant) and an f32
+ *     activation is exact before its one rounding into an f32 sum, with the
+ *     activations' full 24-bit significands; scales, mins and everything after
+ *     them are f32 with FMA.  Only the order of the roundings differs from
+ *     the per-element form (sum (d*sc*q - dmin*m) x is formed as
+ *     d*sc*sum q x - dmin*m*sum x per sub-block).  Results match the exact
+ *     result within |err| <= 1e-3 * sum_j |w_ij x_j| + 1e-6 per GEMV output,
+ *     NaN where the exact computation is NaN (a NaN scale or a NaN
+ *     activation).  Non-finite inputs (Inf scales, non-finite x) give
+ *     non-finite outputs, NaN or Inf.  Activations of magnitude 2^106 (about
+ *     8e31) or more are outside the supported range: the kernels flag them,
+ *     and qmoe_device_status reports QMOE_ERR_UNSUPPORTED.  The many-token
+ *     MoE path (tensor cores) rounds its operands to f16/tf32 (moe_ffn).
  *   - Errors: the status names the class; qmoe_last_error() gives a message
  *     (thread-local) naming the refused argument.
  */
@@ -191,7 +196,10 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  *               overlap on the GPU must not share one
  * Execution: for T >= 32 tokens with Q4_K gate/up and Q6_K down stacks, the
  * tokens are grouped by expert and the expert products run on the tensor
- * cores.  A single token runs one cooperative kernel (one CTA per SM):
+ * cores, whose operands are rounded once: gate/up weights and x (scaled per
+ * token by a power of two) to f16, down weights and the activations to
+ * tf32, so each product carries at most 2 * 2^-11 relative error, inside the
+ * bound above.  A single token runs one cooperative kernel (one CTA per SM):
  * router GEMV, a grid barrier, routing in every CTA, the routed gate/up rows
  * and then the down rows streamed through one pipeline, a second grid barrier
  * before the down products.  2..31 tokens run in cooperative launches of up
@@ -273,7 +281,8 @@ qmoe_status moe_ffn_noalloc(const float* router_W, const void* gate_stack, const
  * word: QMOE_ERR_TIMEOUT if a bounded device wait expired since the last
  * read (a pipeline stage, or a grid barrier that not every CTA reached);
  * QMOE_ERR_UNSUPPORTED if the many-token MoE path met a decoded gate/up
- * weight outside f16 range (its output is then not valid); QMOE_ERR_CUDA if
+ * weight outside f16 range, or a quantized product met an activation of
+ * magnitude 2^106 or more (the output is then not valid); QMOE_ERR_CUDA if
  * the stream reported an error, or if an internal invariant of the routing
  * failed (an expert index outside [0, E) was clamped to 0); else QMOE_OK. */
 qmoe_status qmoe_device_status(void* stream);

@@ -26,7 +26,7 @@
 // The producer warp streams the gate/up tiles and then the down tiles of the
 // CTA through one ring, as in the batch-1 fused kernel.
 //
-// x tables: phase 3 keeps one per token (T * H int16); phase 4 builds the
+// x tables: phase 3 keeps one per token (T * H f32); phase 4 builds the
 // table of one token's activations (k * F values) when the CTA's down units
 // reach that token.  Gate/up tiles hold whole rows (one chunk per tile).
 #pragma once
@@ -180,17 +180,17 @@ struct PairLists {
 // For every pair (t, s) of the tile's expert: act[t][s][f] = w * silu(g) * u.
 template <class Fmt>
 __device__ bool consume_batch_gateup(const StreamParams& p, const Ring& ring, const PairLists& pl,
-                                     const uint32_t* xq, const float* xs, float* part, int T,
+                                     const float* xq, const float* xs, float* part, int T,
                                      float* act, int64_t ubeg, int64_t uend, int& it, int tid) {
     using G = ModeGeom<MODE_GATEUP>;
     constexpr int R = G::R;
     const int v = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
-    const uint4* xq4 = reinterpret_cast<const uint4*>(xq);
+    const float4* xq4 = reinterpret_cast<const float4*>(xq);
     const int ntiles = static_cast<int>((uend - ubeg) / G::TU);
     const int nb = p.nb_seg;
     bool ok = true;
-    uint32_t x[32];
+    float x[64];
     for (int t = 0; t < ntiles; ++t) {
         const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
         const int a = tile_slot<MODE_GATEUP>(p, u0);
@@ -229,7 +229,7 @@ __device__ bool consume_batch_gateup(const StreamParams& p, const Ring& ring, co
             if (ok) {
                 for (int b = v; b < nb; b += G::WK) {
                     const int gidx = tok * nb + b;
-                    load_xq(xq4 + gidx * 32, q, x);
+                    load_xq(xq4 + gidx * 64, q, x);
                     const uint8_t* sbp[R];
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr) sbp[rr] = sbp0[rr] + b * Fmt::SBB;
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     float* rpart = reinterpret_cast<float*>(smem + L.off_rpart);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
-    uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.off_xq);
+    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
     __shared__ int s_abort, s_nact;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     // x tables of every token for the gate/up phase; with H a multiple of
     // 512 the same pass forms the logits of this CTA's first expert
     const bool rmerge = (H % 512) == 0 && cta < E;
-    build_xprime<FmtG, 2>(b.x, T * (H / 256), xq, xs, tid, NC, b.norm_w, 1.f,
+    build_xprime<FmtG, 2>(b.x, T * (H / 256), xq, xs, tid, NC, b.err, b.norm_w, 1.f,
                           b.norm_w ? s_inv : nullptr, H / 16,
                           rmerge ? b.router + static_cast<int64_t>(cta) * H : nullptr, rpart);
     if (rmerge) {
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     tile_range(static_cast<int64_t>(T) * H, cta, ncta, db, de);
     for (int64_t t = db / H; good && db < de; ++t) {
         const int64_t le = de < (t + 1) * H ? de : (t + 1) * H;
-        build_xprime<FmtD, 1>(b.act + t * K * F, K * (F / 256), xq, xs, tid, NC);
+        build_xprime<FmtD, 1>(b.act + t * K * F, K * (F / 256), xq, xs, tid, NC, b.err);
         named_bar(1, NC);
         StreamParams pd = b.dn;
         pd.out = b.residual + t * H;

@@ -4,28 +4,38 @@
 // Q4_0_MATVEC_KERNEL_SRC, Q4_K_MATVEC_KERNEL_SRC with ferrox_q4_k_scale_min,
 // Q5_K_MATVEC_KERNEL_SRC, Q6_K_MATVEC_KERNEL_SRC).
 //
-// Arithmetic scheme (ours, not the pages'):
-//   * The activations are held as 16-bit integers with one f32 scale per
-//     32-element block: x_j ~ s_b * xi_j, s_b = max |x| over the block / 32767,
-//     xi_j = round(x_j / s_b).  The rounding error of every x_j is at most
-//     s_b / 2, 1/65534 of the block's largest |x|.
-//   * The quants stay packed: masks and shifts leave four of them in the
-//     bytes of a word, and dp2a (two 16-bit x times two bytes, summed into
-//     32 bits) multiplies them with the x pairs.  A 32-bit integer sum per
-//     (row, sub-block) is exact (|sum| < 2^26).
-//   * Per sub-block the sum turns into f32 once and takes the block's scales:
-//       sum (d*sc*q - dmin*m) x = d*sc*s_b*sum q xi - dmin*m*sum x
-//     with the offsets and mins applied through sum x over each 16-element
-//     group, computed once per call in f32 from the unrounded x.
+// Arithmetic (f32, as the page kernels: every product is a decoded weight
+// times an f32 activation, summed in f32):
+//   * Every integer quant q in a field [pos, pos+w) of a 32-bit word with
+//     pos + w <= 24 is, reinterpreted as an IEEE binary32 bit pattern,
+//     exactly q * 2^(pos-149) (a subnormal, or a normal with exponent field
+//     1: the mapping bits -> value is linear below 2^24).  One AND isolates
+//     the field; one FFMA against the pre-scaled activation
+//         x'_j = x_j * 2^(128 - E_b - pos_j)
+//     adds q * x_j * 2^-(21 + E_b), exact before its one rounding, into an f32
+//     accumulator.  No int->float conversion, and the activations keep all
+//     24 bits of f32.  (fp32 denormals run at full rate; the library is built
+//     with -ftz=false.)
+//   * E_b is the exponent of the largest |x| of the activation's 32-element
+//     block b (max |x| < 2^E_b), clamped to [1, 106]: x' never overflows, the
+//     products stay normal unless |x_j| is 2^104 below its block's largest,
+//     and the block's de-scale 2^(21 + E_b) is a float.  Blocks holding a
+//     non-finite value take E_b = 1, so NaN and Inf reach the result.
+//     Activations of magnitude 2^106 or more (about 8e31) are outside the
+//     range: the x table flags them (DEV_X_RANGE).
+//   * Per sub-block the sum takes the block's de-scale once, and offsets and
+//     mins are pulled out of the inner loop:
+//         sum (d*sc*q - dmin*m) x = d*sc*sum q x - dmin*m*sum x
+//     with sum x over each 16-element group computed once per call.  Only the
+//     order of rounding differs from the page kernels' per-element form.
 //
 // A lane owns quarter q (0..3) of a 256-element group ("super-block"; for
 // Q8_0/Q4_0, 8 consecutive 32-element blocks).  It processes 64 elements;
-// element i (0..63) of its quarter is elem(q,i) of the group, and 32-bit
-// register k (0..31) of its x block holds elements elem(q,2k) (low half) and
-// elem(q,2k+1) (high half).  The x table is stored in shared memory as
-// uint4 [group][i/8][q] (registers 4p..4p+3 of quarter q in uint4 p), so the
-// four quarter-lanes read 64 contiguous bytes; a lane loads its 32 registers
-// once (load_xq) and applies them to several rows (dotR).
+// element i (0..63) of its quarter is elem(q,i) of the group, and its field
+// sits at bit pos(q,i) once isolated.  x' is stored in shared memory as
+// float4 [group][i/4][q], so the four quarter-lanes read 64 contiguous
+// bytes; a lane loads its 64 values into registers once (load_xq) and
+// applies them to several rows (dotR).
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -38,23 +48,44 @@ __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }
 
-// c + (x pair in xp) . (bytes 0, 1 of w)  /  (bytes 2, 3 of w)
-__device__ __forceinline__ int dp_lo(uint32_t xp, uint32_t w, int c) {
-    return __dp2a_lo(static_cast<int>(xp), static_cast<int>(w), c);
-}
-__device__ __forceinline__ int dp_hi(uint32_t xp, uint32_t w, int c) {
-    return __dp2a_hi(static_cast<int>(xp), static_cast<int>(w), c);
+// Two isolated fields (their bits as floats, q * 2^(pos-149)) times their
+// x' on the packed f32x2 FMA: acc.{x,y} += q{0,1} * x{0,1} * 2^-(21 + E_b).
+__device__ __forceinline__ float2 qfma2(uint32_t m0, uint32_t m1, float x0, float x1,
+                                        float2 acc) {
+    return __ffma2_rn(make_float2(__uint_as_float(m0), __uint_as_float(m1)),
+                      make_float2(x0, x1), acc);
 }
 
-// The 32 x registers of quarter q of one group.
-__device__ __forceinline__ void load_xq(const uint4* xq_group, int q, uint32_t (&x)[32]) {
+// The x table's scales: 2^(128 - E - pos) for an activation of block
+// exponent E whose field sits at bit pos, and the block's de-scale
+// 2^(21 + E); E in [1, 106], pos in [0, 20], so both are normal floats.
+__host__ __device__ __forceinline__ float pow2f(int e) {  // 2^e, -126 <= e <= 127
+#ifdef __CUDA_ARCH__
+    return __int_as_float((127 + e) << 23);
+#else
+    union { int i; float f; } u;
+    u.i = (127 + e) << 23;
+    return u.f;
+#endif
+}
+constexpr int XBLK_EMIN = 1, XBLK_EMAX = 106;
+
+// Bits [24, 24+n) of w isolated at bit 0, on the multiply pipe:
+// (w << (8-n)) keeps them topmost, the high half of * 2^n keeps only them.
+template <int N>
+__device__ __forceinline__ uint32_t top_field(uint32_t w) {
+    return __umulhi(w << (8 - N), 1u << N);
+}
+
+// The 64 x' values of quarter q of one group, from the interleaved table.
+__device__ __forceinline__ void load_xq(const float4* xq_group, int q, float (&x)[64]) {
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const uint4 v = xq_group[p * 4 + q];
-        x[4 * p] = v.x;
-        x[4 * p + 1] = v.y;
-        x[4 * p + 2] = v.z;
-        x[4 * p + 3] = v.w;
+    for (int i4 = 0; i4 < 16; ++i4) {
+        const float4 v = xq_group[i4 * 4 + q];
+        x[4 * i4] = v.x;
+        x[4 * i4 + 1] = v.y;
+        x[4 * i4 + 2] = v.z;
+        x[4 * i4 + 3] = v.w;
     }
 }
 
@@ -72,17 +103,17 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
 }
 
 // Every format provides
-//   elem(q, i)  — the lane element order (64 elements of quarter q);
-//   xslot(e4)   — its inverse on 4-element granules: the slot 4*i4 + q whose
-//                 elements elem(q, 4*i4 .. 4*i4+3) are elements 4*e4 .. 4*e4+3
-//                 of the group (each slot is four consecutive elements);
+//   elem(q, i), pos(q, i)  — the lane element order and extraction offsets;
+//   xslot(e4)   — the inverse of elem on 4-element granules: the slot
+//                 4*i4 + q whose elements elem(q, 4*i4 .. 4*i4+3) are
+//                 elements 4*e4 .. 4*e4+3 of the group;
 //   dotR<R>(sb[R], q, x, xs16, sx, acc[R]) — for R rows whose super-blocks
 //   start at sb[r] (shared memory), adds each row's dot over the lane's
-//   quarter to acc[r]; x: the lane's 32 x registers, xs16: sum x per 16
-//   elements of the group, sx: the group's eight 32-element x scales.
-//   Words of all R rows are loaded first and the element loop runs over words
-//   with the rows innermost, so a lane carries several independent dp2a
-//   chains per row.
+//   quarter to acc[r]; x: the lane's 64 x', xs16: sum x per 16 elements of
+//   the group, sx: the de-scales 2^(21 + E_b) of its eight 32-element blocks.
+//   Words of all R rows are loaded first and the element loop runs over
+//   words with the rows innermost, so a lane carries several independent
+//   FFMA chains.
 
 // ------------------------------------------------------------------ Q4_K
 // 144-byte super-block: f16 d @0, f16 dmin @2, 12 bytes of 6-bit (sc, m)
@@ -91,9 +122,10 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
 // element 64q+32+l (pair 2q+1); value (d*sc)*q - dmin*m.
 //
 // Lane element order: word t (bytes 4t..4t+3), i = 8t + j: j<4 -> low
-// nibble of byte j, j>=4 -> high nibble of byte j-4.  Masking a word with
-// 0x0F0F0F0F (after a shift by 4 for the high nibbles) leaves four quants in
-// its bytes, multiplied by x registers 4t, 4t+1 (low) and 4t+2, 4t+3 (high).
+// nibble of byte j, j>=4 -> high nibble of byte j-4.
+// Extraction per word W: lo b0 &0xF (0), lo b1 &0xF00 (8), lo b2 &0xF0000
+// (16), hi b0 &0xF0 (4), hi b1 &0xF000 (12), hi b2 &0xF00000 (20); byte 3's
+// nibbles come from the multiply pipe (top_field, __umulhi): both at bit 0.
 struct FmtQ4K {
     static constexpr int SBB = 144;
     // Rows may sit at their global stride in shared memory (runs): the
@@ -106,10 +138,16 @@ struct FmtQ4K {
         int t = i >> 3, j = i & 7;
         return j < 4 ? 64 * q + 4 * t + j : 64 * q + 32 + 4 * t + (j - 4);
     }
+    // Inverse of elem on float4 granules: the x' slot (4*i4 + q) holding
+    // elements 4*e4 .. 4*e4+3 of the group.
     __host__ __device__ static int xslot(int e4) {
         const int q = e4 >> 4, r4 = e4 & 15;
         const int i4 = r4 < 8 ? 2 * r4 : 2 * (r4 - 8) + 1;
         return 4 * i4 + q;
+    }
+    __host__ __device__ static int pos(int, int i) {
+        // bit offsets {0, 8, 16, 0, 4, 12, 20, 0} by i % 8, one byte each
+        return static_cast<int>((0x00140C0400100800ull >> (8 * (i & 7))) & 0xFFu);
     }
     // 6-bit (sc, m) of pairs 2q and 2q+1 — the unpacking of
     // ferrox_q4_k_scale_min, four pairs per 32-bit word: pairs 0..3 are the
@@ -133,7 +171,7 @@ struct FmtQ4K {
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const uint32_t (&x)[32], const float* xs16,
+                                                const float (&x)[64], const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         uint32_t W[R][8];
         uint4 h[R];
@@ -145,18 +183,18 @@ struct FmtQ4K {
             W[r][0] = wa.x; W[r][1] = wa.y; W[r][2] = wa.z; W[r][3] = wa.w;
             W[r][4] = wb.x; W[r][5] = wb.y; W[r][6] = wb.z; W[r][7] = wb.w;
         }
-        int ilo[R], ihi[R];
+        float2 alo[R], ahi[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) ilo[r] = ihi[r] = 0;
+        for (int r = 0; r < R; ++r) alo[r] = ahi[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const uint32_t lo = W[r][t] & 0x0F0F0F0Fu, hi = (W[r][t] >> 4) & 0x0F0F0F0Fu;
-                ilo[r] = dp_lo(x[4 * t], lo, ilo[r]);
-                ilo[r] = dp_hi(x[4 * t + 1], lo, ilo[r]);
-                ihi[r] = dp_lo(x[4 * t + 2], hi, ihi[r]);
-                ihi[r] = dp_hi(x[4 * t + 3], hi, ihi[r]);
+                const uint32_t w = W[r][t];
+                alo[r] = qfma2(w & 0xFu, w & 0xF00u, x[8 * t], x[8 * t + 1], alo[r]);
+                alo[r] = qfma2(w & 0xF0000u, top_field<4>(w), x[8 * t + 2], x[8 * t + 3], alo[r]);
+                ahi[r] = qfma2(w & 0xF0u, w & 0xF000u, x[8 * t + 4], x[8 * t + 5], ahi[r]);
+                ahi[r] = qfma2(w & 0xF00000u, __umulhi(w, 16u), x[8 * t + 6], x[8 * t + 7], ahi[r]);
             }
         }
         const float Xa = xs16[4 * q] + xs16[4 * q + 1];
@@ -168,8 +206,9 @@ struct FmtQ4K {
             scale_min(h[r].y, h[r].z, h[r].w, q, sca, ma, scb, mb);
             const float d = f16_bits_to_f32(h[r].x);
             const float dmin = f16_bits_to_f32(h[r].x >> 16);
-            acc[r] += d * fmaf(sca * sa, static_cast<float>(ilo[r]),
-                               scb * sbx * static_cast<float>(ihi[r])) -
+            // (sum of the block's products) * de-scale = sum q x
+            acc[r] += d * fmaf(sca, (alo[r].x + alo[r].y) * sa,
+                               scb * ((ahi[r].x + ahi[r].y) * sbx)) -
                       dmin * fmaf(ma, Xa, mb * Xb);
         }
     }
@@ -178,17 +217,24 @@ struct FmtQ4K {
 // ------------------------------------------------------------------ Q5_K
 // 176-byte super-block: d @0, dmin @2, scales @4, qh[32] @16, qs[128] @48.
 // As Q4_K, plus 16 where bit 2q (low half) / 2q+1 (high half) of qh[l] is
-// set: the qh bit is rotated into bit 4 of each byte and merged with the
-// nibble.  Lane element order as Q4_K.
+// set.  The qh bit is rotated into bit 4 of each byte and merged with the
+// nibble; bits 5..7 of every merged byte are zero, so byte 3's field is
+// one shift.
+// Lane element order as Q4_K; positions: byte k -> 8k for k<3, byte 3's
+// field shifted down -> 0.
 struct FmtQ5K {
     static constexpr int SBB = 176;
     static constexpr bool RUNS_OK = true;
     static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) { return FmtQ4K::elem(q, i); }
     __host__ __device__ static int xslot(int e4) { return FmtQ4K::xslot(e4); }
+    __host__ __device__ static int pos(int, int i) {
+        // bit offsets {0, 8, 16, 0} by i % 4
+        return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
+    }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const uint32_t (&x)[32], const float* xs16,
+                                                const float (&x)[64], const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         const uint32_t rlo = static_cast<uint32_t>(4 - 2 * q) & 31u;
         const uint32_t rhi = static_cast<uint32_t>(3 - 2 * q) & 31u;
@@ -206,9 +252,9 @@ struct FmtQ5K {
             H[r][0] = ha.x; H[r][1] = ha.y; H[r][2] = ha.z; H[r][3] = ha.w;
             H[r][4] = hb.x; H[r][5] = hb.y; H[r][6] = hb.z; H[r][7] = hb.w;
         }
-        int ilo[R], ihi[R];
+        float2 alo[R], ahi[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) ilo[r] = ihi[r] = 0;
+        for (int r = 0; r < R; ++r) alo[r] = ahi[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
 #pragma unroll
@@ -218,10 +264,10 @@ struct FmtQ5K {
                     (w & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rlo) & 0x10101010u);
                 const uint32_t hi =
                     ((w >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rhi) & 0x10101010u);
-                ilo[r] = dp_lo(x[4 * t], lo, ilo[r]);
-                ilo[r] = dp_hi(x[4 * t + 1], lo, ilo[r]);
-                ihi[r] = dp_lo(x[4 * t + 2], hi, ihi[r]);
-                ihi[r] = dp_hi(x[4 * t + 3], hi, ihi[r]);
+                alo[r] = qfma2(lo & 0x1Fu, lo & 0x1F00u, x[8 * t], x[8 * t + 1], alo[r]);
+                alo[r] = qfma2(lo & 0x1F0000u, lo >> 24, x[8 * t + 2], x[8 * t + 3], alo[r]);
+                ahi[r] = qfma2(hi & 0x1Fu, hi & 0x1F00u, x[8 * t + 4], x[8 * t + 5], ahi[r]);
+                ahi[r] = qfma2(hi & 0x1F0000u, hi >> 24, x[8 * t + 6], x[8 * t + 7], ahi[r]);
             }
         }
         const float Xa = xs16[4 * q] + xs16[4 * q + 1];
@@ -233,8 +279,8 @@ struct FmtQ5K {
             FmtQ4K::scale_min(h[r].y, h[r].z, h[r].w, q, sca, ma, scb, mb);
             const float d = f16_bits_to_f32(h[r].x);
             const float dmin = f16_bits_to_f32(h[r].x >> 16);
-            acc[r] += d * fmaf(sca * sa, static_cast<float>(ilo[r]),
-                               scb * sbx * static_cast<float>(ihi[r])) -
+            acc[r] += d * fmaf(sca, (alo[r].x + alo[r].y) * sa,
+                               scb * ((ahi[r].x + ahi[r].y) * sbx)) -
                       dmin * fmaf(ma, Xa, mb * Xb);
         }
     }
@@ -247,10 +293,9 @@ struct FmtQ5K {
 // 2 bits of qh[32h+l]) land at elements 128h + l + {0,32,64,96}, scaled by
 // sc[8h + c + {0,2,4,6}]; value (d*sc)*(q-32).  Super-blocks are only
 // 2-byte aligned, so words are read with funnel shifts.
-// Lane element order: i = 16u + 4t + j -> element 128h + 32t + 16c + 4u + j.
-// The 6-bit values are merged into the bytes of four words v_t (bits 6..7
-// zero), multiplied by x registers 8u + 2t and 8u + 2t + 1; sub-block t (16
-// elements) lies in x block 4h + t.
+// Lane element order: i = 16u + 4t + j -> element 128h + 32t + 16c + 4u + j;
+// positions (0, 8, 16, 0).  The 6-bit values are merged with bits 6..7 of
+// every byte zero, so byte 3's field is one shift.
 struct FmtQ6K {
     static constexpr int SBB = 210;
     static constexpr bool RUNS_OK = true;
@@ -264,6 +309,10 @@ struct FmtQ6K {
     __host__ __device__ static int xslot(int e4) {
         const int h = e4 >> 5, t = (e4 >> 3) & 3, c = (e4 >> 2) & 1, u = e4 & 3;
         return 4 * (4 * u + t) + 2 * h + c;
+    }
+    __host__ __device__ static int pos(int, int i) {
+        // bit offsets {0, 8, 16, 0} by i % 4
+        return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
     }
     // Words [4k, 4k+4) of the 32-byte window (lo, hi), J words plus sh bits in.
     template <int J>
@@ -300,11 +349,11 @@ struct FmtQ6K {
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const uint32_t (&x)[32], const float* xs16,
+                                                const float (&x)[64], const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         if constexpr (R == 4) {
-            // four rows' words beside the x registers exceed the register
-            // budget (168 with nine warps): two passes of two rows, same x
+            // four rows' words beside the 64 x' values exceed the register
+            // budget (168 with nine warps): two passes of two rows, same x'
             const uint8_t* const s0[2] = {sb[0], sb[1]};
             const uint8_t* const s1[2] = {sb[2], sb[3]};
             float a0[2] = {acc[0], acc[1]}, a1[2] = {acc[2], acc[3]};
@@ -358,9 +407,9 @@ struct FmtQ6K {
             sc[r][2] = static_cast<float>(static_cast<int8_t>(s_hi >> (8 * c)));
             sc[r][3] = static_cast<float>(static_cast<int8_t>(s_hi >> (8 * c + 16)));
         }
-        int i0[R], i1[R], i2[R], i3[R];
+        float2 a0[R], a1[R], a2[R], a3[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) i0[r] = i1[r] = i2[r] = i3[r] = 0;
+        for (int r = 0; r < R; ++r) a0[r] = a1[r] = a2[r] = a3[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
 #pragma unroll
@@ -370,11 +419,15 @@ struct FmtQ6K {
                 const uint32_t v1 = (bv & 0x0F0F0F0Fu) | ((hv << 2) & 0x30303030u);
                 const uint32_t v2 = ((av >> 4) & 0x0F0F0F0Fu) | (hv & 0x30303030u);
                 const uint32_t v3 = ((bv >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0x30303030u);
-                const uint32_t* xu = x + 8 * u;
-                i0[r] = dp_hi(xu[1], v0, dp_lo(xu[0], v0, i0[r]));
-                i1[r] = dp_hi(xu[3], v1, dp_lo(xu[2], v1, i1[r]));
-                i2[r] = dp_hi(xu[5], v2, dp_lo(xu[4], v2, i2[r]));
-                i3[r] = dp_hi(xu[7], v3, dp_lo(xu[6], v3, i3[r]));
+                const float* xu = x + 16 * u;
+                a0[r] = qfma2(v0 & 0x3Fu, v0 & 0x3F00u, xu[0], xu[1], a0[r]);
+                a0[r] = qfma2(v0 & 0x3F0000u, v0 >> 24, xu[2], xu[3], a0[r]);
+                a1[r] = qfma2(v1 & 0x3Fu, v1 & 0x3F00u, xu[4], xu[5], a1[r]);
+                a1[r] = qfma2(v1 & 0x3F0000u, v1 >> 24, xu[6], xu[7], a1[r]);
+                a2[r] = qfma2(v2 & 0x3Fu, v2 & 0x3F00u, xu[8], xu[9], a2[r]);
+                a2[r] = qfma2(v2 & 0x3F0000u, v2 >> 24, xu[10], xu[11], a2[r]);
+                a3[r] = qfma2(v3 & 0x3Fu, v3 & 0x3F00u, xu[12], xu[13], a3[r]);
+                a3[r] = qfma2(v3 & 0x3F0000u, v3 >> 24, xu[14], xu[15], a3[r]);
             }
         }
         // 16-element groups of this lane: 8h + 2t + c; x blocks 4h + t
@@ -383,10 +436,10 @@ struct FmtQ6K {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float d32 = -32.f * d[r];
-            float res = sc[r][0] * fmaf(d32, X[0], XS[0] * d[r] * static_cast<float>(i0[r]));
-            res = fmaf(sc[r][1], fmaf(d32, X[2], XS[1] * d[r] * static_cast<float>(i1[r])), res);
-            res = fmaf(sc[r][2], fmaf(d32, X[4], XS[2] * d[r] * static_cast<float>(i2[r])), res);
-            res = fmaf(sc[r][3], fmaf(d32, X[6], XS[3] * d[r] * static_cast<float>(i3[r])), res);
+            float res = sc[r][0] * fmaf(d32, X[0], (a0[r].x + a0[r].y) * XS[0] * d[r]);
+            res = fmaf(sc[r][1], fmaf(d32, X[2], (a1[r].x + a1[r].y) * XS[1] * d[r]), res);
+            res = fmaf(sc[r][2], fmaf(d32, X[4], (a2[r].x + a2[r].y) * XS[2] * d[r]), res);
+            res = fmaf(sc[r][3], fmaf(d32, X[6], (a3[r].x + a3[r].y) * XS[3] * d[r]), res);
             acc[r] += res;
         }
     }
@@ -395,18 +448,23 @@ struct FmtQ6K {
 // ------------------------------------------------------------------ Q8_0
 // 34-byte blocks: f16 d, 32 int8; value d*q.  A group of 8 blocks is 272
 // bytes; quarter q holds blocks 2q, 2q+1 at byte 68q (4-byte aligned when
-// the group is).  The signed quants go to dp2a as they are stored.
-// Lane element order: i = 32k + j -> element 64q + 32k + j; block k's words
-// t = 0..7 meet x registers 16k + 2t, 16k + 2t + 1.
+// the group is).  q+128 is extracted as an unsigned byte (XOR 0x80) and the
+// 128*sum(x) offset removed per block.
+// Lane element order: i = 32k + 4t + j -> element 64q + 32k + 4t + j;
+// positions (0, 8, 16, 0).
 struct FmtQ80 {
     static constexpr int SBB = 272;
     static constexpr bool RUNS_OK = false;
     static constexpr int SLOT_REM128 = -1;
     __host__ __device__ static int elem(int q, int i) { return 64 * q + i; }
     __host__ __device__ static int xslot(int e4) { return 4 * (e4 & 15) + (e4 >> 4); }
+    __host__ __device__ static int pos(int, int i) {
+        // bit offsets {0, 8, 16, 0} by i % 4
+        return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
+    }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const uint32_t (&x)[32], const float* xs16,
+                                                const float (&x)[64], const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         uint32_t U[R][17];
 #pragma unroll
@@ -415,27 +473,34 @@ struct FmtQ80 {
 #pragma unroll
             for (int k = 0; k < 17; ++k) U[r][k] = u[k];
         }
-        int iA[R], iB[R];
+        float2 aA[R], aB[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) iA[r] = iB[r] = 0;
+        for (int r = 0; r < R; ++r) aA[r] = aB[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                // block A's quants start 2 bytes into the quarter, block B's
-                // 4-byte aligned at byte 36
                 const uint32_t wa = __funnelshift_r(U[r][t], U[r][t + 1], 16);
                 const uint32_t wb = U[r][9 + t];
-                iA[r] = dp_hi(x[2 * t + 1], wa, dp_lo(x[2 * t], wa, iA[r]));
-                iB[r] = dp_hi(x[17 + 2 * t], wb, dp_lo(x[16 + 2 * t], wb, iB[r]));
+                aA[r] = qfma2((wa ^ 0x80808080u) & 0xFFu, (wa ^ 0x80808080u) & 0xFF00u, x[4 * t],
+                              x[4 * t + 1], aA[r]);
+                aA[r] = qfma2((wa ^ 0x80808080u) & 0xFF0000u, __umulhi(wa + 0x80000000u, 256u),
+                              x[4 * t + 2], x[4 * t + 3], aA[r]);
+                aB[r] = qfma2((wb ^ 0x80808080u) & 0xFFu, (wb ^ 0x80808080u) & 0xFF00u,
+                              x[32 + 4 * t], x[33 + 4 * t], aB[r]);
+                aB[r] = qfma2((wb ^ 0x80808080u) & 0xFF0000u, __umulhi(wb + 0x80000000u, 256u),
+                              x[34 + 4 * t], x[35 + 4 * t], aB[r]);
             }
         }
+        const float XA = xs16[4 * q] + xs16[4 * q + 1];
+        const float XB = xs16[4 * q + 2] + xs16[4 * q + 3];
         const float sA = sx[2 * q], sB = sx[2 * q + 1];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float dA = f16_bits_to_f32(U[r][0]);
             const float dB = f16_bits_to_f32(U[r][8] >> 16);
-            acc[r] += fmaf(dA * sA, static_cast<float>(iA[r]), dB * sB * static_cast<float>(iB[r]));
+            acc[r] += dA * fmaf(aA[r].x + aA[r].y, sA, -128.f * XA) +
+                      dB * fmaf(aB[r].x + aB[r].y, sB, -128.f * XB);
         }
     }
 };
@@ -445,8 +510,7 @@ struct FmtQ80 {
 // nibble element i+16; value (nibble-8)*d.  A group of 8 blocks is 144
 // bytes; quarter q holds blocks 2q, 2q+1 at byte 36q.
 // Lane element order: i = 32k + 8t + j: j<4 -> element 32(2q+k) + 4t + j,
-// j>=4 -> element 32(2q+k) + 16 + 4t + (j-4): word t of block k meets x
-// registers 16k + 4t, +1 (low nibbles) and 16k + 4t + 2, +3 (high nibbles).
+// j>=4 -> element 32(2q+k) + 16 + 4t + (j-4); positions as Q4_K.
 struct FmtQ40 {
     static constexpr int SBB = 144;
     static constexpr bool RUNS_OK = false;
@@ -461,9 +525,10 @@ struct FmtQ40 {
         const int i4 = 8 * (blk & 1) + 2 * (r & 3) + (r >= 4 ? 1 : 0);
         return 4 * i4 + (blk >> 1);
     }
+    __host__ __device__ static int pos(int q, int i) { return FmtQ4K::pos(q, i); }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const uint32_t (&x)[32], const float* xs16,
+                                                const float (&x)[64], const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         uint32_t U[R][9];
 #pragma unroll
@@ -472,21 +537,22 @@ struct FmtQ40 {
 #pragma unroll
             for (int k = 0; k < 9; ++k) U[r][k] = u[k];
         }
-        int ia[R][2];
+        float2 a[R][2];
 #pragma unroll
-        for (int r = 0; r < R; ++r) ia[r][0] = ia[r][1] = 0;
+        for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const int o = 16 * k + 4 * t;
+                const int o = 32 * k + 8 * t;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const uint32_t w = k == 0 ? __funnelshift_r(U[r][t], U[r][t + 1], 16)
                                               : U[r][5 + t];
-                    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
-                    ia[r][k] = dp_hi(x[o + 1], lo, dp_lo(x[o], lo, ia[r][k]));
-                    ia[r][k] = dp_hi(x[o + 3], hi, dp_lo(x[o + 2], hi, ia[r][k]));
+                    a[r][k] = qfma2(w & 0xFu, w & 0xF00u, x[o], x[o + 1], a[r][k]);
+                    a[r][k] = qfma2(w & 0xF0000u, top_field<4>(w), x[o + 2], x[o + 3], a[r][k]);
+                    a[r][k] = qfma2(w & 0xF0u, w & 0xF000u, x[o + 4], x[o + 5], a[r][k]);
+                    a[r][k] = qfma2(w & 0xF00000u, __umulhi(w, 16u), x[o + 6], x[o + 7], a[r][k]);
                 }
             }
         }
@@ -497,8 +563,8 @@ struct FmtQ40 {
         for (int r = 0; r < R; ++r) {
             const float dA = f16_bits_to_f32(U[r][0]);
             const float dB = f16_bits_to_f32(U[r][4] >> 16);
-            acc[r] += dA * fmaf(sA, static_cast<float>(ia[r][0]), -8.f * XA) +
-                      dB * fmaf(sB, static_cast<float>(ia[r][1]), -8.f * XB);
+            acc[r] += dA * fmaf(a[r][0].x + a[r][0].y, sA, -8.f * XA) +
+                      dB * fmaf(a[r][1].x + a[r][1].y, sB, -8.f * XB);
         }
     }
 };

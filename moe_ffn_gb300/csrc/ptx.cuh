@@ -8,7 +8,13 @@ namespace qmoe {
 
 // Device error codes: the first one recorded wins; read and cleared by
 // qmoe_device_status().
-enum : unsigned { DEV_OK = 0, DEV_TIMEOUT_FULL = 1, DEV_TIMEOUT_EMPTY = 2, DEV_ROUTE_RANGE = 5 };
+enum : unsigned {
+    DEV_OK = 0,
+    DEV_TIMEOUT_FULL = 1,
+    DEV_TIMEOUT_EMPTY = 2,
+    DEV_ROUTE_RANGE = 5,  // an expert index was clamped (internal invariant)
+    DEV_X_RANGE = 6       // an activation of magnitude >= 2^106
+};
 
 // The device control block, one per device (a global of the library): the
 // error word, the limit of every bounded wait, and a fault-injection setting

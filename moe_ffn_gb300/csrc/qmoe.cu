@@ -1109,6 +1109,10 @@ qmoe_status qmoe_device_status(void* stream) {
             return fail(QMOE_ERR_UNSUPPORTED,
                         "a decoded gate/up weight is outside f16 range (code %u); the "
                         "many-token path cannot represent it", v);
+        if (v == DEV_X_RANGE)
+            return fail(QMOE_ERR_UNSUPPORTED,
+                        "an activation of magnitude 2^106 or more reached a quantized product "
+                        "(code %u); its output is not valid", v);
         if (v == DEV_ROUTE_RANGE)
             return fail(QMOE_ERR_CUDA,
                         "internal error: the routing produced an expert index outside [0, E) "

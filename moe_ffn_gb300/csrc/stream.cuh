@@ -7,10 +7,10 @@
 // mbarrier).  Warps 0..7 are consumers.  A tile holds 8*R row slots; lane
 // (g = lane/4, q = lane%4) owns slots rr*8 + g (rr < R) and quarter q of each
 // 256-element group its warp is given: warp v takes groups v, v+8, ... of
-// the chunk.  A lane loads its 32 x registers of a group (64 activations as
-// 16-bit integers, formats.cuh) once and applies them to its R rows.  Per-row partial sums are reduced by
-// shuffles across the four quarters and through shared memory across warps,
-// in a fixed order (deterministic).
+// the chunk.  A lane loads its 64 pre-scaled f32 activations of a group
+// (formats.cuh) into registers once and applies them to its R rows.  Per-row
+// partial sums are reduced by shuffles across the four quarters and through
+// shared memory across warps, in a fixed order (deterministic).
 //
 // Weight operands are read-only constants: the producer starts streaming
 // them before griddepcontrol.wait, so a launch overlaps the tail of the
@@ -81,10 +81,10 @@ template <int MODE> struct ModeGeom {
     static constexpr int WK = NCW;                         // warps along K
 };
 
-// The x table of one 256-element group: 32 x registers per quarter lane
-// (int16 pairs, uint4 [8][4]), and beside it in the xs region 16 sums of x
-// (one per 16 elements) then the 8 block scales.
-constexpr int XQ_GROUP_BYTES = 512;
+// The x table of one 256-element group: the 64 pre-scaled activations x' of
+// each quarter lane (float4 [16][4]), and beside it in the xs region 16 sums
+// of x (one per 16 elements) then the 8 block de-scales 2^(21 + E_b).
+constexpr int XQ_GROUP_BYTES = 1024;
 constexpr int XS_GROUP_FLOATS = 24;
 constexpr int XS_GROUP_BYTES = 4 * XS_GROUP_FLOATS;
 
@@ -218,21 +218,25 @@ __device__ inline float rms_inverse(const float* __restrict__ h, int n, float ep
 }
 
 template <class Fmt, int UNR = 4>
-__device__ inline void build_xprime(const float* __restrict__ x, int ngroups, uint32_t* xq,
-                                    float* xs, int tid, int nthreads,
+__device__ inline void build_xprime(const float* __restrict__ x, int ngroups, float* xq,
+                                    float* xs, int tid, int nthreads, DevCtl* err,
                                     const float* __restrict__ nw = nullptr, float inv = 1.f,
                                     const float* inv_tok = nullptr, int tok_n16 = 0,
                                     const float* __restrict__ rrow = nullptr,
                                     float* rpart = nullptr) {
-    // The x table (see formats.cuh): x as 16-bit integers in the lanes'
-    // register order, one scale per 32-element block (max |x| / 32767; NaN if
-    // the block holds a non-finite value, so that it reaches the result), and
-    // the f32 sum of x per 16 elements.  A thread takes 16-element chunks of
-    // x: it loads the chunk's four aligned float4s (all loads in flight
-    // before any use, so the table costs one L2 round trip), takes the block
-    // maximum with its neighbour (the chunk pair 2m, 2m+1 is block m),
-    // rounds, and scatters each granule of four to its slot (the formats'
-    // element orders keep every slot four consecutive elements).
+    // The x table (see formats.cuh): x' = x * 2^(128 - E_b - pos) in the
+    // lanes' register order, with E_b the exponent of the largest |x| of the
+    // 32-element block (clamped to [1, 106]; 1 for a block holding a
+    // non-finite value), the block's de-scale 2^(21 + E_b), and the f32 sum
+    // of x per 16 elements.  Multiplying by a power of two is exact: x' holds
+    // every bit of x.  A thread takes 16-element chunks of x: it loads the
+    // chunk's four aligned float4s (all loads in flight before any use, so
+    // the table costs one L2 round trip), takes the block maximum with its
+    // neighbour (the chunk pair 2m, 2m+1 is block m), and scatters each
+    // granule of four to its slot (the formats' element orders keep every
+    // slot four consecutive elements), each element scaled for its field's
+    // bit position.  A block whose largest |x| is 2^106 or more is outside
+    // the range and is flagged (DEV_X_RANGE).
     // With nw, the table is of the normed input x_j * inv * nw_j (ffn_norm).
     // With inv_tok, x holds several tokens of tok_n16 chunks each, token t
     // normed with inv_tok[t] (nw applies per token).  UNR chunks per thread
@@ -245,7 +249,8 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, ui
     const int n16 = ngroups * 16;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const float4* r4 = reinterpret_cast<const float4*>(rrow);
-    uint2* xq2 = reinterpret_cast<uint2*>(xq);
+    float4* xq4 = reinterpret_cast<float4*>(xq);
+    bool range = false;
     // warps step together (the shuffles below need every lane of the warp,
     // also those whose chunks are past the end): nthreads is a multiple of 32
     for (int wbase = tid & ~31; wbase < n16; wbase += nthreads * UNR) {
@@ -315,29 +320,35 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, ui
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             bad = __shfl_xor_sync(0xffffffffu, static_cast<int>(bad), 1) != 0 || bad;
             if (c < n16) {
-                const float qs = (bad || mx == 0.f) ? 0.f : 32767.f / mx;
+                // mx < 2^E for E = its biased exponent - 126
+                int E = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 126;
+                if (bad) E = XBLK_EMIN;
+                if (E < XBLK_EMIN) E = XBLK_EMIN;
+                if (E > XBLK_EMAX) {
+                    E = XBLK_EMAX;
+                    range = true;
+                }
                 float s = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) s += (v[u][k].x + v[u][k].y) + (v[u][k].z + v[u][k].w);
                 const int g = c >> 4;
                 xs[g * XS_GROUP_FLOATS + (c & 15)] = s;
-                if ((c & 1) == 0)
-                    xs[g * XS_GROUP_FLOATS + 16 + ((c & 15) >> 1)] =
-                        bad ? __int_as_float(0x7FC00000) : mx * (1.0f / 32767.f);
+                if ((c & 1) == 0) xs[g * XS_GROUP_FLOATS + 16 + ((c & 15) >> 1)] = pow2f(21 + E);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int slot = Fmt::xslot(4 * (c & 15) + k);
-                    const int q = slot & 3, i4 = slot >> 2;
-                    const uint32_t e0 = static_cast<uint16_t>(__float2int_rn(v[u][k].x * qs));
-                    const uint32_t e1 = static_cast<uint16_t>(__float2int_rn(v[u][k].y * qs));
-                    const uint32_t e2 = static_cast<uint16_t>(__float2int_rn(v[u][k].z * qs));
-                    const uint32_t e3 = static_cast<uint16_t>(__float2int_rn(v[u][k].w * qs));
-                    xq2[(g * 32 + (i4 >> 1) * 4 + q) * 2 + (i4 & 1)] =
-                        make_uint2(e0 | (e1 << 16), e2 | (e3 << 16));
+                    const int q = slot & 3, i = 4 * (slot >> 2);
+                    float4 o;
+                    o.x = v[u][k].x * pow2f(128 - E - Fmt::pos(q, i));
+                    o.y = v[u][k].y * pow2f(128 - E - Fmt::pos(q, i + 1));
+                    o.z = v[u][k].z * pow2f(128 - E - Fmt::pos(q, i + 2));
+                    o.w = v[u][k].w * pow2f(128 - E - Fmt::pos(q, i + 3));
+                    xq4[g * 64 + slot] = o;
                 }
             }
         }
     }
+    if (range) record_error(err, DEV_X_RANGE);
 }
 
 // Address of the bytes of (row slot r, k-segment ks) for the tile starting
@@ -577,20 +588,20 @@ __device__ bool produce_phase(const StreamParams& p, const Ring& ring, const int
 // unless every warp's data for it arrived.
 template <class Fmt, int MODE>
 __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int32_t* s_idx,
-                              const float* s_w, const uint32_t* xq, const float* xs, float* part,
+                              const float* s_w, const float* xq, const float* xs, float* part,
                               int64_t ubeg, int64_t uend, int& it, int tid) {
     using G = ModeGeom<MODE>;
     constexpr int R = G::R;
     const int v = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
-    const uint4* xq4 = reinterpret_cast<const uint4*>(xq);
+    const float4* xq4 = reinterpret_cast<const float4*>(xq);
     const int ntiles = static_cast<int>((uend - ubeg + G::TU - 1) / G::TU);
     bool ok = true;
     // Gate/up tiles with K <= 8 groups give a warp the same group in every
-    // tile: its x registers stay loaded.  Elsewhere groups change each call,
-    // and keeping them live would only cost registers.
+    // tile: its x' stays in registers.  Elsewhere groups change each call,
+    // and keeping x' live would only cost registers.
     constexpr bool KEEP_X = MODE == MODE_GATEUP;
-    uint32_t x[32];
+    float x[64];
     int xg = -1;
     for (int t = 0; t < ntiles; ++t) {
         const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
@@ -634,7 +645,7 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
                 const int ks = cd.ks0 + pk, b = cd.b0 + bb;
                 const int gidx = ks * p.nb_seg + b;
                 if (!KEEP_X || gidx != xg) {
-                    load_xq(xq4 + gidx * 32, q, x);
+                    load_xq(xq4 + gidx * 64, q, x);
                     xg = gidx;
                 }
                 const float* xsg = xs + gidx * XS_GROUP_FLOATS;
@@ -717,7 +728,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
     uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + L.off_logit);
     float* part = reinterpret_cast<float*>(smem + L.off_part);
     float* xs = reinterpret_cast<float*>(smem + L.off_xs);
-    uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.off_xq);
+    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int64_t ubeg, uend;
@@ -763,7 +774,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
         pdl_wait();
         pdl_trigger();
     }
-    build_xprime<Fmt>(p.x, p.nb_seg * p.n_kseg, xq, xs, tid, NCW * 32);
+    build_xprime<Fmt>(p.x, p.nb_seg * p.n_kseg, xq, xs, tid, NCW * 32, p.err);
     named_bar(1, NCW * 32);
     if (!p.moe) named_bar(2, NTHREADS);  // the stage barriers are initialised
     consume_phase<Fmt, MODE>(p, ring, s_idx, s_w, xq, xs, part, ubeg, uend, it, tid);

@@ -75,9 +75,9 @@ def test_qmv_sweep_workload(qm, orc, qt):
 
 @pytest.mark.parametrize("qt", QTS, ids=lambda q: QNAME[q])
 def test_qmv_wide_range_x(qm, orc, qt):
-    """The activations are rounded to 16 bits per 32-element block.  Blocks
-    whose values span six decades (one value 1e3, the rest ~1e-3, random
-    signs) still meet the stated bound, with margin."""
+    """Blocks whose activations span six decades (one value 1e3, the rest
+    ~1e-3, random signs): the products take every bit of each f32 x, so the
+    small values are not lost beside the large one."""
     g = synth.rng(900 + qt)
     rows, cols = 300, 2048
     W = synth.quant_matrix(g, qt, rows, cols)
@@ -85,13 +85,59 @@ def test_qmv_wide_range_x(qm, orc, qt):
     x[g.integers(0, 32, cols // 32) + np.arange(0, cols, 32)] = 1e3 * np.sign(g.standard_normal(cols // 32))
     y = gpu_qmv(qm, qt, W, rows, cols, x)
     ref, sabs = orc.matvec(qt, W, rows, cols, x, with_sabs=True)
-    assert check_gemv(y, ref, sabs, f"wide-range x {QNAME[qt]}") < 0.5
+    assert check_gemv(y, ref, sabs, f"wide-range x {QNAME[qt]}") < 0.05
+
+
+@pytest.mark.parametrize("qt", [synth.Q4_0, synth.Q8_0], ids=lambda q: QNAME[q])
+def test_qmv_outlier_on_zero_weight_column(qm, orc, qt):
+    """x[0] = 1e3 inside an N(0,1) block, on a column whose weight is zero in
+    every row (Q4_0 nibble 8, Q8_0 quant 0); the other blocks ~1e-3.  The
+    bound 1e-3 * sum |w x| then holds no term of the outlier, so an
+    activation rounded relative to its block's largest value would miss it;
+    with f32 activations every row meets it with a wide margin."""
+    g = synth.rng(4242 + qt)
+    rows, cols = 256, 2048
+    W = synth.quant_matrix(g, qt, rows, cols)
+    if qt == synth.Q4_0:
+        W[:, 2] = (W[:, 2] & 0xF0) | 0x08  # block 0, element 0: low nibble of byte 2
+    else:
+        W[:, 2] = 0                        # block 0, element 0: int8 quant at byte 2
+    x = (synth.normal(g, cols) * 1e-3).astype(np.float32)
+    x[:32] = synth.normal(g, 32)
+    x[0] = 1e3
+    y = gpu_qmv(qm, qt, W, rows, cols, x)
+    ref, sabs = orc.matvec(qt, W, rows, cols, x, with_sabs=True)
+    assert np.all(orc.dequant(qt, W, rows, cols)[:, 0] == 0)
+    assert check_gemv(y, ref, sabs, f"outlier on a zero column {QNAME[qt]}") < 0.05
+
+
+@pytest.mark.parametrize("qt", QTS, ids=lambda q: QNAME[q])
+def test_qmv_activation_range(qm, orc, qt):
+    """Activations from 1e-30 to 1e30 in one vector (blocks of very different
+    magnitude, and values 2^40 apart inside one block): each product keeps
+    its full precision.  Values of 2^106 and more are outside the range and
+    reported as UNSUPPORTED by the device status."""
+    g = synth.rng(77 + qt)
+    rows, cols = 64, 2048
+    W = synth.quant_matrix(g, qt, rows, cols)
+    x = synth.normal(g, cols)
+    x *= (10.0 ** g.integers(-30, 31, cols // 32)).repeat(32).astype(np.float32)
+    x[5::32] *= 2.0 ** -40
+    y = gpu_qmv(qm, qt, W, rows, cols, x)
+    assert qm.device_status() == qm.OK
+    ref, sabs = orc.matvec(qt, W, rows, cols, x, with_sabs=True)
+    assert check_gemv(y, ref, sabs, f"activation range {QNAME[qt]}") < 0.05
+    x[100] = 2.0 ** 107
+    gpu_qmv(qm, qt, W, rows, cols, x)
+    assert qm.device_status() == qm.ERR_UNSUPPORTED
+    assert "2^106" in qm.last_error()
+    assert qm.device_status() == qm.OK
 
 
 @pytest.mark.parametrize("qt", QTS, ids=lambda q: QNAME[q])
 def test_qmv_nan_x_reaches_every_row(qm, orc, qt):
     """A NaN activation makes every output NaN (each row multiplies it), as in
-    the oracle: the rounded block carries a NaN scale."""
+    the oracle."""
     g = synth.rng(950 + qt)
     rows, cols = 64, 1024
     W = synth.quant_matrix(g, qt, rows, cols)
