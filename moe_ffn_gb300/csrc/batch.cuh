@@ -190,7 +190,6 @@ __device__ bool consume_batch_gateup(const StreamParams& p, const Ring& ring, co
     const int ntiles = static_cast<int>((uend - ubeg) / G::TU);
     const int nb = p.nb_seg;
     bool ok = true;
-    float x[64];
     for (int t = 0; t < ntiles; ++t) {
         const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
         const int a = tile_slot<MODE_GATEUP>(p, u0);
@@ -229,12 +228,11 @@ __device__ bool consume_batch_gateup(const StreamParams& p, const Ring& ring, co
             if (ok) {
                 for (int b = v; b < nb; b += G::WK) {
                     const int gidx = tok * nb + b;
-                    load_xq(xq4 + gidx * 64, q, x);
                     const uint8_t* sbp[R];
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr) sbp[rr] = sbp0[rr] + b * Fmt::SBB;
                     const float* xsg = xs + gidx * XS_GROUP_FLOATS;
-                    Fmt::template dotR<R>(sbp, q, x, xsg, xsg + 16, acc);
+                    Fmt::template dotR<R>(sbp, q, xq4 + gidx * 64 + q, xsg, xsg + 16, acc);
                 }
             }
 #pragma unroll

@@ -34,8 +34,8 @@
 // element i (0..63) of its quarter is elem(q,i) of the group, and its field
 // sits at bit pos(q,i) once isolated.  x' is stored in shared memory as
 // float4 [group][i/4][q], so the four quarter-lanes read 64 contiguous
-// bytes; a lane loads its 64 values into registers once (load_xq) and
-// applies them to several rows (dotR).
+// bytes; the element loop of dotR loads the x' of each word as it goes and
+// applies them to several rows.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -77,17 +77,11 @@ __device__ __forceinline__ uint32_t top_field(uint32_t w) {
     return __umulhi(w << (8 - N), 1u << N);
 }
 
-// The 64 x' values of quarter q of one group, from the interleaved table.
-__device__ __forceinline__ void load_xq(const float4* xq_group, int q, float (&x)[64]) {
-#pragma unroll
-    for (int i4 = 0; i4 < 16; ++i4) {
-        const float4 v = xq_group[i4 * 4 + q];
-        x[4 * i4] = v.x;
-        x[4 * i4 + 1] = v.y;
-        x[4 * i4 + 2] = v.z;
-        x[4 * i4 + 3] = v.w;
-    }
-}
+// A lane's x' values of one group: xg = (the group's float4 table) + q, so
+// that its elements 4*i4 .. 4*i4+3 are xg[4 * i4].  Each format's element
+// loop loads the four or eight x' it needs next from shared memory (a
+// broadcast to the eight row lanes of each quarter) and applies them to all
+// R rows, so no lane holds its 64 x' in registers.
 
 // Read 4 consecutive 32-bit words starting at a 2-byte-aligned shared-memory
 // address: aligned loads plus a funnel shift by 0 or 16 bits.
@@ -107,9 +101,9 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
 //   xslot(e4)   — the inverse of elem on 4-element granules: the slot
 //                 4*i4 + q whose elements elem(q, 4*i4 .. 4*i4+3) are
 //                 elements 4*e4 .. 4*e4+3 of the group;
-//   dotR<R>(sb[R], q, x, xs16, sx, acc[R]) — for R rows whose super-blocks
+//   dotR<R>(sb[R], q, xg, xs16, sx, acc[R]) — for R rows whose super-blocks
 //   start at sb[r] (shared memory), adds each row's dot over the lane's
-//   quarter to acc[r]; x: the lane's 64 x', xs16: sum x per 16 elements of
+//   quarter to acc[r]; xg: the lane's x' (above), xs16: sum x per 16 elements of
 //   the group, sx: the de-scales 2^(21 + E_b) of its eight 32-element blocks.
 //   Words of all R rows are loaded first and the element loop runs over
 //   words with the rows innermost, so a lane carries several independent
@@ -171,7 +165,7 @@ struct FmtQ4K {
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const float (&x)[64], const float* xs16,
+                                                const float4* __restrict__ xg, const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         uint32_t W[R][8];
         uint4 h[R];
@@ -188,13 +182,14 @@ struct FmtQ4K {
         for (int r = 0; r < R; ++r) alo[r] = ahi[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
+            const float4 xa = xg[8 * t], xb = xg[8 * t + 4];  // elements 8t .. 8t+7
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t w = W[r][t];
-                alo[r] = qfma2(w & 0xFu, w & 0xF00u, x[8 * t], x[8 * t + 1], alo[r]);
-                alo[r] = qfma2(w & 0xF0000u, top_field<4>(w), x[8 * t + 2], x[8 * t + 3], alo[r]);
-                ahi[r] = qfma2(w & 0xF0u, w & 0xF000u, x[8 * t + 4], x[8 * t + 5], ahi[r]);
-                ahi[r] = qfma2(w & 0xF00000u, __umulhi(w, 16u), x[8 * t + 6], x[8 * t + 7], ahi[r]);
+                alo[r] = qfma2(w & 0xFu, w & 0xF00u, xa.x, xa.y, alo[r]);
+                alo[r] = qfma2(w & 0xF0000u, top_field<4>(w), xa.z, xa.w, alo[r]);
+                ahi[r] = qfma2(w & 0xF0u, w & 0xF000u, xb.x, xb.y, ahi[r]);
+                ahi[r] = qfma2(w & 0xF00000u, __umulhi(w, 16u), xb.z, xb.w, ahi[r]);
             }
         }
         const float Xa = xs16[4 * q] + xs16[4 * q + 1];
@@ -234,7 +229,7 @@ struct FmtQ5K {
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const float (&x)[64], const float* xs16,
+                                                const float4* __restrict__ xg, const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         const uint32_t rlo = static_cast<uint32_t>(4 - 2 * q) & 31u;
         const uint32_t rhi = static_cast<uint32_t>(3 - 2 * q) & 31u;
@@ -257,6 +252,7 @@ struct FmtQ5K {
         for (int r = 0; r < R; ++r) alo[r] = ahi[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
+            const float4 xa = xg[8 * t], xb = xg[8 * t + 4];  // elements 8t .. 8t+7
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t w = W[r][t], hw = H[r][t];
@@ -264,10 +260,10 @@ struct FmtQ5K {
                     (w & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rlo) & 0x10101010u);
                 const uint32_t hi =
                     ((w >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(hw, hw, rhi) & 0x10101010u);
-                alo[r] = qfma2(lo & 0x1Fu, lo & 0x1F00u, x[8 * t], x[8 * t + 1], alo[r]);
-                alo[r] = qfma2(lo & 0x1F0000u, lo >> 24, x[8 * t + 2], x[8 * t + 3], alo[r]);
-                ahi[r] = qfma2(hi & 0x1Fu, hi & 0x1F00u, x[8 * t + 4], x[8 * t + 5], ahi[r]);
-                ahi[r] = qfma2(hi & 0x1F0000u, hi >> 24, x[8 * t + 6], x[8 * t + 7], ahi[r]);
+                alo[r] = qfma2(lo & 0x1Fu, lo & 0x1F00u, xa.x, xa.y, alo[r]);
+                alo[r] = qfma2(lo & 0x1F0000u, lo >> 24, xa.z, xa.w, alo[r]);
+                ahi[r] = qfma2(hi & 0x1Fu, hi & 0x1F00u, xb.x, xb.y, ahi[r]);
+                ahi[r] = qfma2(hi & 0x1F0000u, hi >> 24, xb.z, xb.w, ahi[r]);
             }
         }
         const float Xa = xs16[4 * q] + xs16[4 * q + 1];
@@ -349,16 +345,18 @@ struct FmtQ6K {
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const float (&x)[64], const float* xs16,
+                                                const float4* __restrict__ xg, const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         if constexpr (R == 4) {
-            // four rows' words beside the 64 x' values exceed the register
-            // budget (168 with nine warps): two passes of two rows, same x'
+            // four rows' words at once exceed the register budget: two
+            // passes of two rows, the second's loads after the first's
+            // arithmetic
             const uint8_t* const s0[2] = {sb[0], sb[1]};
             const uint8_t* const s1[2] = {sb[2], sb[3]};
             float a0[2] = {acc[0], acc[1]}, a1[2] = {acc[2], acc[3]};
-            dotR<2>(s0, q, x, xs16, sx, a0);
-            dotR<2>(s1, q, x, xs16, sx, a1);
+            dotR<2>(s0, q, xg, xs16, sx, a0);
+            asm volatile("" ::: "memory");
+            dotR<2>(s1, q, xg, xs16, sx, a1);
             acc[0] = a0[0];
             acc[1] = a0[1];
             acc[2] = a1[0];
@@ -412,6 +410,9 @@ struct FmtQ6K {
         for (int r = 0; r < R; ++r) a0[r] = a1[r] = a2[r] = a3[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
+            // elements 16u .. 16u+15
+            const float4 x0 = xg[16 * u], x1 = xg[16 * u + 4], x2 = xg[16 * u + 8],
+                         x3 = xg[16 * u + 12];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t av = A[r][u], bv = B[r][u], hv = H[r][u];
@@ -419,15 +420,14 @@ struct FmtQ6K {
                 const uint32_t v1 = (bv & 0x0F0F0F0Fu) | ((hv << 2) & 0x30303030u);
                 const uint32_t v2 = ((av >> 4) & 0x0F0F0F0Fu) | (hv & 0x30303030u);
                 const uint32_t v3 = ((bv >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0x30303030u);
-                const float* xu = x + 16 * u;
-                a0[r] = qfma2(v0 & 0x3Fu, v0 & 0x3F00u, xu[0], xu[1], a0[r]);
-                a0[r] = qfma2(v0 & 0x3F0000u, v0 >> 24, xu[2], xu[3], a0[r]);
-                a1[r] = qfma2(v1 & 0x3Fu, v1 & 0x3F00u, xu[4], xu[5], a1[r]);
-                a1[r] = qfma2(v1 & 0x3F0000u, v1 >> 24, xu[6], xu[7], a1[r]);
-                a2[r] = qfma2(v2 & 0x3Fu, v2 & 0x3F00u, xu[8], xu[9], a2[r]);
-                a2[r] = qfma2(v2 & 0x3F0000u, v2 >> 24, xu[10], xu[11], a2[r]);
-                a3[r] = qfma2(v3 & 0x3Fu, v3 & 0x3F00u, xu[12], xu[13], a3[r]);
-                a3[r] = qfma2(v3 & 0x3F0000u, v3 >> 24, xu[14], xu[15], a3[r]);
+                a0[r] = qfma2(v0 & 0x3Fu, v0 & 0x3F00u, x0.x, x0.y, a0[r]);
+                a0[r] = qfma2(v0 & 0x3F0000u, v0 >> 24, x0.z, x0.w, a0[r]);
+                a1[r] = qfma2(v1 & 0x3Fu, v1 & 0x3F00u, x1.x, x1.y, a1[r]);
+                a1[r] = qfma2(v1 & 0x3F0000u, v1 >> 24, x1.z, x1.w, a1[r]);
+                a2[r] = qfma2(v2 & 0x3Fu, v2 & 0x3F00u, x2.x, x2.y, a2[r]);
+                a2[r] = qfma2(v2 & 0x3F0000u, v2 >> 24, x2.z, x2.w, a2[r]);
+                a3[r] = qfma2(v3 & 0x3Fu, v3 & 0x3F00u, x3.x, x3.y, a3[r]);
+                a3[r] = qfma2(v3 & 0x3F0000u, v3 >> 24, x3.z, x3.w, a3[r]);
             }
         }
         // 16-element groups of this lane: 8h + 2t + c; x blocks 4h + t
@@ -464,7 +464,7 @@ struct FmtQ80 {
     }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const float (&x)[64], const float* xs16,
+                                                const float4* __restrict__ xg, const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         uint32_t U[R][17];
 #pragma unroll
@@ -478,18 +478,19 @@ struct FmtQ80 {
         for (int r = 0; r < R; ++r) aA[r] = aB[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
+            const float4 xa = xg[4 * t], xb = xg[32 + 4 * t];  // elements 4t.., 32+4t..
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t wa = __funnelshift_r(U[r][t], U[r][t + 1], 16);
                 const uint32_t wb = U[r][9 + t];
-                aA[r] = qfma2((wa ^ 0x80808080u) & 0xFFu, (wa ^ 0x80808080u) & 0xFF00u, x[4 * t],
-                              x[4 * t + 1], aA[r]);
+                aA[r] = qfma2((wa ^ 0x80808080u) & 0xFFu, (wa ^ 0x80808080u) & 0xFF00u, xa.x,
+                              xa.y, aA[r]);
                 aA[r] = qfma2((wa ^ 0x80808080u) & 0xFF0000u, __umulhi(wa + 0x80000000u, 256u),
-                              x[4 * t + 2], x[4 * t + 3], aA[r]);
-                aB[r] = qfma2((wb ^ 0x80808080u) & 0xFFu, (wb ^ 0x80808080u) & 0xFF00u,
-                              x[32 + 4 * t], x[33 + 4 * t], aB[r]);
+                              xa.z, xa.w, aA[r]);
+                aB[r] = qfma2((wb ^ 0x80808080u) & 0xFFu, (wb ^ 0x80808080u) & 0xFF00u, xb.x,
+                              xb.y, aB[r]);
                 aB[r] = qfma2((wb ^ 0x80808080u) & 0xFF0000u, __umulhi(wb + 0x80000000u, 256u),
-                              x[34 + 4 * t], x[35 + 4 * t], aB[r]);
+                              xb.z, xb.w, aB[r]);
             }
         }
         const float XA = xs16[4 * q] + xs16[4 * q + 1];
@@ -528,7 +529,7 @@ struct FmtQ40 {
     __host__ __device__ static int pos(int q, int i) { return FmtQ4K::pos(q, i); }
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
-                                                const float (&x)[64], const float* xs16,
+                                                const float4* __restrict__ xg, const float* xs16,
                                                 const float* sx, float (&acc)[R]) {
         uint32_t U[R][9];
 #pragma unroll
@@ -544,15 +545,16 @@ struct FmtQ40 {
         for (int k = 0; k < 2; ++k) {
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const int o = 32 * k + 8 * t;
+                const int o = 32 * k + 8 * t;  // elements o .. o+7
+                const float4 xa = xg[o], xb = xg[o + 4];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const uint32_t w = k == 0 ? __funnelshift_r(U[r][t], U[r][t + 1], 16)
                                               : U[r][5 + t];
-                    a[r][k] = qfma2(w & 0xFu, w & 0xF00u, x[o], x[o + 1], a[r][k]);
-                    a[r][k] = qfma2(w & 0xF0000u, top_field<4>(w), x[o + 2], x[o + 3], a[r][k]);
-                    a[r][k] = qfma2(w & 0xF0u, w & 0xF000u, x[o + 4], x[o + 5], a[r][k]);
-                    a[r][k] = qfma2(w & 0xF00000u, __umulhi(w, 16u), x[o + 6], x[o + 7], a[r][k]);
+                    a[r][k] = qfma2(w & 0xFu, w & 0xF00u, xa.x, xa.y, a[r][k]);
+                    a[r][k] = qfma2(w & 0xF0000u, top_field<4>(w), xa.z, xa.w, a[r][k]);
+                    a[r][k] = qfma2(w & 0xF0u, w & 0xF000u, xb.x, xb.y, a[r][k]);
+                    a[r][k] = qfma2(w & 0xF00000u, __umulhi(w, 16u), xb.z, xb.w, a[r][k]);
                 }
             }
         }

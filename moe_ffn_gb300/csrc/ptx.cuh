@@ -116,7 +116,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Programmatic dependent launch.
+// Programmatic dependent launch.  Every kernel triggers its dependents right
+// after its own wait: the next launch on the stream is then scheduled while
+// this one runs, and its CTAs start (and stream their weights) as soon as
+// they fit; its own griddepcontrol.wait holds back every read of this
+// launch's outputs until this grid has completed and its writes are
+// visible.  Triggering at the very start was measured slower on the GEMV
+// sweep: the next launch's copies then compete with this launch's own.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -94,6 +94,7 @@ struct DevInfo {
     bool supported = false;
     int sms = 0;
     int smem_optin = 0;
+    int smem_pair = 0;  // dynamic shared memory per CTA that lets two CTAs share an SM
     DevCtl* err = nullptr;
     int cc_major = 0, cc_minor = 0;
 };
@@ -115,6 +116,8 @@ static qmoe_status device_info(DevInfo** out) {
         d.cc_minor = prop.minor;
         d.sms = prop.multiProcessorCount;
         d.smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+        d.smem_pair = static_cast<int>(prop.sharedMemPerMultiprocessor / 2 -
+                                       prop.reservedSharedMemPerBlock);
         d.supported = (prop.major == 10 && prop.minor == 3);
         if (d.supported) {
             void* p = nullptr;
@@ -153,30 +156,38 @@ static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cud
 // Plan chunking and pipeline depth for a streamed GEMV; false if it cannot
 // fit in shared memory.
 template <class Fmt, int MODE>
-static bool plan(StreamParams& p, int smem_optin, int grid, int* smem_bytes) {
+static bool plan(StreamParams& p, int smem_optin, int smem_pair, int grid, int* smem_bytes) {
     using G = ModeGeom<MODE>;
     p.stage_bytes = 0;
     p.nstages = 0;
-    const int room = smem_optin - smem_layout(p).total;
-    // A CTA with a single tile gains nothing from a ring: one stage may then
-    // hold the whole tile (whole rows, so few and large copies).  Otherwise
-    // the stage budget is at most 96 KB, and two stages must fit beside the
-    // x table.
+    const int fixed0 = smem_layout(p).total;
+    // A CTA with a single tile gains nothing from a ring: one stage then
+    // holds the whole tile (whole rows, so few and large copies).  Where that
+    // stage fits in smem_pair bytes, two CTAs share an SM: the next launch's
+    // CTAs then stream their weights while this launch still computes.
+    // Otherwise the stage budget is at most 96 KB, and two stages must fit
+    // beside the x table.
     const int64_t per_cta = (p.units + grid - 1) / grid;
     const bool one_tile = per_cta <= G::TU;
-    bool planned = false;
     if (one_tile) {
-        planned = plan_chunks<Fmt, MODE>(p, room) && p.n_chunk == 1;
+        const int rows = static_cast<int>(per_cta);
+        for (const int cap : {smem_pair, smem_optin}) {
+            if (cap - fixed0 > 0 && plan_chunks<Fmt, MODE>(p, cap - fixed0, rows) &&
+                p.n_chunk == 1) {
+                p.nstages = 1;
+                *smem_bytes = smem_layout(p).total;
+                if (*smem_bytes <= cap) return true;
+            }
+            p.nstages = 0;
+        }
     }
-    if (!planned) {
-        const int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
-        if (!plan_chunks<Fmt, MODE>(p, budget)) return false;
-    }
-    p.nstages = 0;
+    const int room = smem_optin - fixed0;
+    const int budget = room / 2 < 96 * 1024 ? room / 2 : 96 * 1024;
+    if (!plan_chunks<Fmt, MODE>(p, budget)) return false;
     const int fixed = smem_layout(p).total;
     int ns = (smem_optin - fixed) / p.stage_bytes;
     if (ns > MAX_STAGES) ns = MAX_STAGES;
-    if (ns < (planned ? 1 : 2)) return false;
+    if (ns < 2) return false;
     p.nstages = ns;
     *smem_bytes = smem_layout(p).total;
     return true;
@@ -188,7 +199,7 @@ static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st)
     const int64_t grid = p.units < d.sms ? p.units : d.sms;
     p.uq = p.units / grid;
     p.ur = static_cast<int>(p.units % grid);
-    if (!plan<Fmt, MODE>(p, d.smem_optin, static_cast<int>(grid), &smem))
+    if (!plan<Fmt, MODE>(p, d.smem_optin, d.smem_pair, static_cast<int>(grid), &smem))
         return fail(QMOE_ERR_UNSUPPORTED,
                     "K = %d x %d groups of 256 does not fit the shared-memory pipeline",
                     p.n_kseg, p.nb_seg);
@@ -198,6 +209,11 @@ static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st)
     cudaGetDevice(&dev);
     if (smem > configured_smem[dev & 63]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // the whole unified L1 as shared memory: two CTAs of this kernel, or
+        // of two consecutive launches, can then share an SM
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         configured_smem[dev & 63] = smem;
     }

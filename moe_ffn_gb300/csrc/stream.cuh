@@ -7,10 +7,11 @@
 // mbarrier).  Warps 0..7 are consumers.  A tile holds 8*R row slots; lane
 // (g = lane/4, q = lane%4) owns slots rr*8 + g (rr < R) and quarter q of each
 // 256-element group its warp is given: warp v takes groups v, v+8, ... of
-// the chunk.  A lane loads its 64 pre-scaled f32 activations of a group
-// (formats.cuh) into registers once and applies them to its R rows.  Per-row
-// partial sums are reduced by shuffles across the four quarters and through
-// shared memory across warps, in a fixed order (deterministic).
+// the chunk.  A lane reads its pre-scaled f32 activations of a group
+// (formats.cuh) from shared memory word by word and applies each to its R
+// rows.  Per-row partial sums are reduced by shuffles across the four
+// quarters and through shared memory across warps, in a fixed order
+// (deterministic).
 //
 // Weight operands are read-only constants: the producer starts streaming
 // them before griddepcontrol.wait, so a launch overlaps the tail of the
@@ -259,6 +260,7 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
         float4 rv[UNR][4];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
+            if (wbase + u * nthreads >= n16) break;  // warp-uniform: no lane of the warp has work
             const int c = base + u * nthreads;
             if (c < n16) {
 #pragma unroll
@@ -292,6 +294,7 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
         }
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
+            if (wbase + u * nthreads >= n16) break;  // warp-uniform, as above
             const int c = base + u * nthreads;
             if (rrow && c - (c & 31) < n16) {  // whole warps: all lanes valid
                 float d = 0.f;
@@ -597,12 +600,6 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
     const float4* xq4 = reinterpret_cast<const float4*>(xq);
     const int ntiles = static_cast<int>((uend - ubeg + G::TU - 1) / G::TU);
     bool ok = true;
-    // Gate/up tiles with K <= 8 groups give a warp the same group in every
-    // tile: its x' stays in registers.  Elsewhere groups change each call,
-    // and keeping x' live would only cost registers.
-    constexpr bool KEEP_X = MODE == MODE_GATEUP;
-    float x[64];
-    int xg = -1;
     for (int t = 0; t < ntiles; ++t) {
         const int64_t u0 = ubeg + static_cast<int64_t>(G::TU) * t;
         const int s0 = tile_slot<MODE>(p, u0);
@@ -616,7 +613,9 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             acc[rr] = 0.f;
-            const int r = rr * 8 + g;
+            // a QMV slot past the CTA's last row reads slot 0 (the stage may
+            // hold only the CTA's rows); its sum is never written
+            const int r = (MODE == MODE_QMV && u0 + rr * 8 + g >= uend) ? 0 : rr * 8 + g;
             int h = r;
             if (p.runs) {
                 const RunSlot rs = run_of<MODE>(p, u0, s0, r);
@@ -644,10 +643,6 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
                 const int pk = tt / cd.nbp, bb = tt - pk * cd.nbp;
                 const int ks = cd.ks0 + pk, b = cd.b0 + bb;
                 const int gidx = ks * p.nb_seg + b;
-                if (!KEEP_X || gidx != xg) {
-                    load_xq(xq4 + gidx * 64, q, x);
-                    xg = gidx;
-                }
                 const float* xsg = xs + gidx * XS_GROUP_FLOATS;
                 const uint32_t ksoff =
                     (MODE == MODE_DOWN && p.moe)
@@ -661,7 +656,7 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
                     const int delta = static_cast<int>((rowlo[rr] + ksoff + b0off) & 15u);
                     sbp[rr] = st + rowoff[rr] + pk * p.piece_stride + delta + bb * Fmt::SBB;
                 }
-                Fmt::template dotR<R>(sbp, q, x, xsg, xsg + 16, acc);
+                Fmt::template dotR<R>(sbp, q, xq4 + gidx * 64 + q, xsg, xsg + 16, acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ring.empty[s]);
@@ -713,8 +708,18 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
     return ok;
 }
 
+// QMV launches are bounded to two CTAs per SM (96 registers with nine warps
+// per CTA: the register file is split between the four sub-partitions), so
+// the next launch's CTAs can stream their weights beside this one.  Q6_K
+// needs more registers than that without spilling and keeps one per SM.
 template <class Fmt, int MODE>
-__global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamParams p) {
+constexpr int stream_min_blocks() {
+    return (MODE == MODE_QMV && Fmt::SBB != 210) ? 2 : 1;
+}
+
+template <class Fmt, int MODE>
+__global__ void __launch_bounds__(NTHREADS, (stream_min_blocks<Fmt, MODE>())) stream_gemv_kernel(
+    const StreamParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = smem_layout(p);
     Ring ring;
@@ -746,17 +751,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
         }
         fence_barrier_init();
     }
-    // Routing decides which expert rows are streamed.  The down product's
-    // logits come from the router kernel two launches back, complete before
-    // this grid was allowed to start; the gate/up kernel reads them right
-    // after its own dependency wait.
-    if (p.moe && MODE == MODE_DOWN) {
-        route_topk(p.logits, p.E, p.topk, s_key, s_idx, s_w, tid, NTHREADS, 0, p.renorm, p.err);
-    } else if (p.moe && MODE == MODE_GATEUP) {
+    // Routing decides which expert rows are streamed.  The logits come from
+    // the router kernel, one launch back (gate/up) or two (down); the wait
+    // covers both, since the launch in between waited for the router before
+    // it could complete.
+    if (p.moe) {
         pdl_wait();
         pdl_trigger();
         route_topk(p.logits, p.E, p.topk, s_key, s_idx, s_w, tid, NTHREADS, 0, p.renorm, p.err);
-        if (blockIdx.x == 0 && tid < p.topk) {
+        if (MODE == MODE_GATEUP && blockIdx.x == 0 && tid < p.topk) {
             if (p.topk_idx_out) p.topk_idx_out[tid] = s_idx[tid];
             if (p.topk_w_out) p.topk_w_out[tid] = s_w[tid];
         }
@@ -770,7 +773,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
         produce_phase<Fmt, MODE>(p, ring, s_idx, ubeg, uend, it, lane);
         return;
     }
-    if (!(p.moe && MODE == MODE_GATEUP)) {  // the MoE gate/up grid waited above
+    if (!p.moe) {  // the MoE grids waited above
         pdl_wait();
         pdl_trigger();
     }
@@ -783,11 +786,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
 // ------------------------------------------------------------ host planning
 // Chunk geometry of a streamed phase for a stage budget (bytes): how rows
 // are cut into chunks, the slot strides and the bytes one stage needs.
-// False if not even one group per row fits.
+// A stage holds `rows` row slots: all G::ROWS of a tile, or (QMV, when every
+// CTA has a single tile) just the rows one CTA owns — its consumers then
+// read slot 0 for the tile's unused slots.  False if not even one group per
+// row fits.
 template <class Fmt, int MODE>
-inline bool plan_chunks(StreamParams& p, int budget) {
+inline bool plan_chunks(StreamParams& p, int budget, int rows = ModeGeom<MODE>::ROWS) {
     using G = ModeGeom<MODE>;
-    if (budget < G::ROWS * (Fmt::SBB + 31)) return false;
+    if (MODE != MODE_QMV || rows > G::ROWS || rows < 1) rows = G::ROWS;
+    if (budget < rows * (Fmt::SBB + 31)) return false;
     const int seg_full = p.nb_seg * Fmt::SBB;
     // Whole k-segments fit: runs of consecutive rows, one bulk copy each.
     // A k-segment region holds the tile's rows at their global stride plus
@@ -796,7 +803,7 @@ inline bool plan_chunks(StreamParams& p, int budget) {
     // Rows of 2 KB and more stream at the full rate as separate copies, so
     // formats whose loads would conflict at the global stride keep padded
     // per-row slots for them.
-    const int run_piece = align_up(G::ROWS * seg_full, 16) + 144;
+    const int run_piece = align_up(rows * seg_full, 16) + 144;
     if (run_piece <= budget && (Fmt::RUNS_OK || seg_full < 2048)) {
         p.runs = 1;
         p.n_sbc = 1;
@@ -811,19 +818,19 @@ inline bool plan_chunks(StreamParams& p, int budget) {
     p.runs = 0;
     const int piece_full = align_up(seg_full + 15, 16);
     int nbp_max;
-    if (G::ROWS * p.n_kseg * piece_full <= budget) {
+    if (rows * p.n_kseg * piece_full <= budget) {
         p.n_sbc = 1;
         p.chunk_ks = p.n_kseg;
         p.chunk_sb = p.nb_seg;
         nbp_max = p.nb_seg;
-    } else if (G::ROWS * piece_full <= budget) {
+    } else if (rows * piece_full <= budget) {
         p.n_sbc = 1;
-        p.chunk_ks = budget / (G::ROWS * piece_full);
+        p.chunk_ks = budget / (rows * piece_full);
         p.chunk_sb = p.nb_seg;
         nbp_max = p.nb_seg;
     } else {
         p.chunk_ks = 1;
-        int csb = (budget / G::ROWS - 31) / Fmt::SBB;
+        int csb = (budget / rows - 31) / Fmt::SBB;
         if (csb >= G::WK) csb -= csb % G::WK;
         if (csb < 1) csb = 1;
         p.chunk_sb = csb;
@@ -836,7 +843,7 @@ inline bool plan_chunks(StreamParams& p, int budget) {
         p.slot_stride += (Fmt::SLOT_REM128 - p.slot_stride % 128 + 128) % 128;
     else if (p.slot_stride % 32 == 0)
         p.slot_stride += 16;  // alternate rows across bank halves
-    p.stage_bytes = G::ROWS * p.slot_stride;
+    p.stage_bytes = rows * p.slot_stride;
     p.n_chunk = (p.n_sbc == 1) ? (p.n_kseg + p.chunk_ks - 1) / p.chunk_ks : p.n_kseg * p.n_sbc;
     return true;
 }
