@@ -465,6 +465,37 @@ def bench_layers(qm, synth, dev, stream, args):
     del G, U, D, gf
     torch.cuda.empty_cache()
 
+    # lm_head-sized GEMVs: vocab 151,936 x hidden 2048, F32 (1.24 GB) and
+    # Q6_K (255 MB, two copies rotating)
+    lm = {}
+    V, Hd = 151936, 2048
+    for name, qt in (("F32", 0), ("Q6_K", 5), ("Q8_0", 1)):
+        g = synth.rng(151936 + qt)
+        if qt == 0:
+            Wl = torch.randn((V, Hd), device=dev) * 0.02
+            nbytes = Wl.numel() * 4
+            cps = [Wl]
+        else:
+            Wh = synth.quant_matrix(g, qt, V, Hd)
+            nbytes = Wh.nbytes
+            cps = [torch.from_numpy(Wh).to(dev) for _ in range(2)]
+        xl = torch.from_numpy(synth.normal(g, Hd)).to(dev)
+        yl = torch.empty(V, device=dev)
+
+        def lcall(i, qt=qt, cps=cps, xl=xl, yl=yl):
+            qm.qmv(qt, cps[i % len(cps)], V, Hd, xl, yl)
+        nl = 4
+        gl = capture(torch, lcall, nl)
+        gl.replay()
+        us = time_graph(torch, gl) * 1e3 / nl
+        alg = nbytes + 4 * Hd + 4 * V
+        lm[name] = {"us": round(us, 2), "gbs": round(alg / us / 1e3, 1),
+                    "frac": round(alg / us / 1e3 / peak, 3), "bytes": alg}
+        del gl, cps
+        torch.cuda.empty_cache()
+    out["lm_head_gemv"] = {"workload": "vocab 151936 x hidden 2048, one qmv call",
+                           "launch": "CUDA graph of 4 calls, >= 0.5 s, median", **lm}
+
     # MoE 512-token layer
     shp = synth.MOE_PREFILL
     inp = synth.moe_inputs(0, **shp)

@@ -112,8 +112,10 @@ typedef struct {
  *   qtype  one of qmoe_qtype (F32 included: a plain f32 GEMV)
  *   W      [rows][row_bytes] blocks, 16-byte aligned, read-only
  *   rows   >= 1;  cols >= 1, a multiple of the format's block elements
- *          (32 or 256; else INVALID_ARGUMENT) and, for quantized formats, of
- *          256 (else UNSUPPORTED); cols <= 32768
+ *          (F32: 4, else UNSUPPORTED; Q8_0/Q4_0: 32; K-quants: 256; else
+ *          INVALID_ARGUMENT); cols <= 32768.  Q8_0/Q4_0 rows of an odd
+ *          number of blocks are 2-byte aligned in W (row_bytes = cols/32*34
+ *          or *18): the rows follow each other unpadded, as GGUF stores them
  *   x      [cols] f32, 16-byte aligned;  y [rows] f32, overwritten
  * Errors: INVALID_ARGUMENT (null, sizes, alignment), UNSUPPORTED (qtype,
  * cols, device not sm_103), CUDA. */

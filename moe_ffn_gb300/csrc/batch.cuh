@@ -232,7 +232,7 @@ __device__ bool consume_batch_gateup(const StreamParams& p, const Ring& ring, co
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr) sbp[rr] = sbp0[rr] + b * Fmt::SBB;
                     const float* xsg = xs + gidx * XS_GROUP_FLOATS;
-                    Fmt::template dotR<R>(sbp, q, xq4 + gidx * 64 + q, xsg, xsg + 16, acc);
+                    Fmt::template dotR<R>(sbp, q, xq4 + gidx * 64 + q, xsg, xsg + 16, 8, acc);
                 }
             }
 #pragma unroll
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     // x tables of every token for the gate/up phase; with H a multiple of
     // 512 the same pass forms the logits of this CTA's first expert
     const bool rmerge = (H % 512) == 0 && cta < E;
-    build_xprime<FmtG, 2>(b.x, T * (H / 256), xq, xs, tid, NC, b.err, b.norm_w, 1.f,
+    build_xprime<FmtG, 2>(b.x, T * (H / 256), T * (H / 16), xq, xs, tid, NC, b.err, b.norm_w, 1.f,
                           b.norm_w ? s_inv : nullptr, H / 16,
                           rmerge ? b.router + static_cast<int64_t>(cta) * H : nullptr, rpart);
     if (rmerge) {
@@ -556,7 +556,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_batch_kernel(const BatchParam
     tile_range(static_cast<int64_t>(T) * H, cta, ncta, db, de);
     for (int64_t t = db / H; good && db < de; ++t) {
         const int64_t le = de < (t + 1) * H ? de : (t + 1) * H;
-        build_xprime<FmtD, 1>(b.act + t * K * F, K * (F / 256), xq, xs, tid, NC, b.err);
+        build_xprime<FmtD, 1>(b.act + t * K * F, K * (F / 256), K * (F / 16), xq, xs, tid, NC,
+                              b.err);
         named_bar(1, NC);
         StreamParams pd = b.dn;
         pd.out = b.residual + t * H;

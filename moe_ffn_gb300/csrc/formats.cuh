@@ -96,15 +96,41 @@ __device__ __forceinline__ void load4_u16al(const uint8_t* p, uint32_t (&w)[4]) 
     for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(r[k], r[k + 1], sh);
 }
 
+// N consecutive 32-bit words from a 2-byte-aligned shared-memory address.
+// Rows of whole 256-element groups are 4-byte aligned (plain loads); a
+// Q8_0/Q4_0 row of an odd number of 32-element blocks is only 2-byte
+// aligned, and its words are funnel-shifted out of aligned loads (one word
+// more, inside the stage's slack).
+template <int N>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[N]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+    if ((a & 2u) == 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) w[k] = u[k];
+    } else {
+        uint32_t prev = u[0];
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            const uint32_t next = u[k + 1];
+            w[k] = __funnelshift_r(prev, next, 16);
+            prev = next;
+        }
+    }
+}
+
 // Every format provides
 //   elem(q, i), pos(q, i)  — the lane element order and extraction offsets;
 //   xslot(e4)   — the inverse of elem on 4-element granules: the slot
 //                 4*i4 + q whose elements elem(q, 4*i4 .. 4*i4+3) are
 //                 elements 4*e4 .. 4*e4+3 of the group;
-//   dotR<R>(sb[R], q, xg, xs16, sx, acc[R]) — for R rows whose super-blocks
-//   start at sb[r] (shared memory), adds each row's dot over the lane's
-//   quarter to acc[r]; xg: the lane's x' (above), xs16: sum x per 16 elements of
-//   the group, sx: the de-scales 2^(21 + E_b) of its eight 32-element blocks.
+//   dotR<R>(sb[R], q, xg, xs16, sx, nblk, acc[R]) — for R rows whose
+//   super-blocks start at sb[r] (shared memory), adds each row's dot over the
+//   lane's quarter to acc[r]; xg: the lane's x' (above), xs16: sum x per 16
+//   elements of the group, sx: the de-scales 2^(21 + E_b) of its eight
+//   32-element blocks; nblk: the group's valid 32-element blocks (8, or fewer
+//   for the partial last group of a Q8_0/Q4_0 row; the other formats always
+//   have 8).
 //   Words of all R rows are loaded first and the element loop runs over
 //   words with the rows innermost, so a lane carries several independent
 //   FFMA chains.
@@ -166,7 +192,7 @@ struct FmtQ4K {
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
-                                                const float* sx, float (&acc)[R]) {
+                                                const float* sx, int nblk, float (&acc)[R]) {
         uint32_t W[R][8];
         uint4 h[R];
 #pragma unroll
@@ -230,7 +256,7 @@ struct FmtQ5K {
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
-                                                const float* sx, float (&acc)[R]) {
+                                                const float* sx, int nblk, float (&acc)[R]) {
         const uint32_t rlo = static_cast<uint32_t>(4 - 2 * q) & 31u;
         const uint32_t rhi = static_cast<uint32_t>(3 - 2 * q) & 31u;
         uint32_t W[R][8], H[R][8];
@@ -346,7 +372,7 @@ struct FmtQ6K {
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
-                                                const float* sx, float (&acc)[R]) {
+                                                const float* sx, int nblk, float (&acc)[R]) {
         if constexpr (R == 4) {
             // four rows' words at once exceed the register budget: two
             // passes of two rows, the second's loads after the first's
@@ -354,9 +380,9 @@ struct FmtQ6K {
             const uint8_t* const s0[2] = {sb[0], sb[1]};
             const uint8_t* const s1[2] = {sb[2], sb[3]};
             float a0[2] = {acc[0], acc[1]}, a1[2] = {acc[2], acc[3]};
-            dotR<2>(s0, q, xg, xs16, sx, a0);
+            dotR<2>(s0, q, xg, xs16, sx, nblk, a0);
             asm volatile("" ::: "memory");
-            dotR<2>(s1, q, xg, xs16, sx, a1);
+            dotR<2>(s1, q, xg, xs16, sx, nblk, a1);
             acc[0] = a0[0];
             acc[1] = a0[1];
             acc[2] = a1[0];
@@ -448,7 +474,7 @@ struct FmtQ6K {
 // ------------------------------------------------------------------ Q8_0
 // 34-byte blocks: f16 d, 32 int8; value d*q.  A group of 8 blocks is 272
 // bytes; quarter q holds blocks 2q, 2q+1 at byte 68q (4-byte aligned when
-// the group is).  q+128 is extracted as an unsigned byte (XOR 0x80) and the
+// the group is; a row of an odd number of blocks is 2-byte aligned).  q+128 is extracted as an unsigned byte (XOR 0x80) and the
 // 128*sum(x) offset removed per block.
 // Lane element order: i = 32k + 4t + j -> element 64q + 32k + 4t + j;
 // positions (0, 8, 16, 0).
@@ -465,14 +491,10 @@ struct FmtQ80 {
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
-                                                const float* sx, float (&acc)[R]) {
+                                                const float* sx, int nblk, float (&acc)[R]) {
         uint32_t U[R][17];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t* u = reinterpret_cast<const uint32_t*>(sb[r] + 68 * q);
-#pragma unroll
-            for (int k = 0; k < 17; ++k) U[r][k] = u[k];
-        }
+        for (int r = 0; r < R; ++r) load_words<17>(sb[r] + 68 * q, U[r]);
         float2 aA[R], aB[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) aA[r] = aB[r] = make_float2(0.f, 0.f);
@@ -496,12 +518,15 @@ struct FmtQ80 {
         const float XA = xs16[4 * q] + xs16[4 * q + 1];
         const float XB = xs16[4 * q + 2] + xs16[4 * q + 3];
         const float sA = sx[2 * q], sB = sx[2 * q + 1];
+        // blocks past a partial group's end hold stale bytes: selected away
+        const bool okA = 2 * q < nblk, okB = 2 * q + 1 < nblk;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float dA = f16_bits_to_f32(U[r][0]);
             const float dB = f16_bits_to_f32(U[r][8] >> 16);
-            acc[r] += dA * fmaf(aA[r].x + aA[r].y, sA, -128.f * XA) +
-                      dB * fmaf(aB[r].x + aB[r].y, sB, -128.f * XB);
+            const float vA = dA * fmaf(aA[r].x + aA[r].y, sA, -128.f * XA);
+            const float vB = dB * fmaf(aB[r].x + aB[r].y, sB, -128.f * XB);
+            acc[r] += (okA ? vA : 0.f) + (okB ? vB : 0.f);
         }
     }
 };
@@ -530,14 +555,10 @@ struct FmtQ40 {
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
-                                                const float* sx, float (&acc)[R]) {
+                                                const float* sx, int nblk, float (&acc)[R]) {
         uint32_t U[R][9];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t* u = reinterpret_cast<const uint32_t*>(sb[r] + 36 * q);
-#pragma unroll
-            for (int k = 0; k < 9; ++k) U[r][k] = u[k];
-        }
+        for (int r = 0; r < R; ++r) load_words<9>(sb[r] + 36 * q, U[r]);
         float2 a[R][2];
 #pragma unroll
         for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = make_float2(0.f, 0.f);
@@ -561,12 +582,15 @@ struct FmtQ40 {
         const float XA = xs16[4 * q] + xs16[4 * q + 1];
         const float XB = xs16[4 * q + 2] + xs16[4 * q + 3];
         const float sA = sx[2 * q], sB = sx[2 * q + 1];
+        // blocks past a partial group's end hold stale bytes: selected away
+        const bool okA = 2 * q < nblk, okB = 2 * q + 1 < nblk;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float dA = f16_bits_to_f32(U[r][0]);
             const float dB = f16_bits_to_f32(U[r][4] >> 16);
-            acc[r] += dA * fmaf(a[r][0].x + a[r][0].y, sA, -8.f * XA) +
-                      dB * fmaf(a[r][1].x + a[r][1].y, sB, -8.f * XB);
+            const float vA = dA * fmaf(a[r][0].x + a[r][0].y, sA, -8.f * XA);
+            const float vB = dB * fmaf(a[r][1].x + a[r][1].y, sB, -8.f * XB);
+            acc[r] += (okA ? vA : 0.f) + (okB ? vB : 0.f);
         }
     }
 };

@@ -225,7 +225,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fused_ffn_kernel(const FusedParam
         f.norm_w ? rms_inverse(f.gu.x, f.gu.nb_seg * 256, f.eps, red, tid, NC, 1) : 1.f;
     // with H a multiple of 512 the x-table pass also forms this CTA's first logit
     const bool rmerge = f.moe && (f.H % 512) == 0 && cta < f.E;
-    build_xprime<FmtG, 2>(f.gu.x, f.gu.nb_seg, xq, xs, tid, NC, f.err, f.norm_w, inv, nullptr,
+    build_xprime<FmtG, 2>(f.gu.x, f.gu.nb_seg, f.gu.nb_seg * 16, xq, xs, tid, NC, f.err, f.norm_w,
+                          inv, nullptr,
                           f.H / 16, rmerge ? f.router + cta * f.H : nullptr, rpart);
     if (f.moe) {
         if (rmerge) {
@@ -301,7 +302,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fused_ffn_kernel(const FusedParam
         if (tid == 0) sync_invalidate(f.sync);
         return;
     }
-    build_xprime<FmtD>(f.dn.x, f.dn.nb_seg * f.dn.n_kseg, xq, xs, tid, NC, f.err);
+    build_xprime<FmtD>(f.dn.x, f.dn.nb_seg * f.dn.n_kseg, f.dn.nb_seg * f.dn.n_kseg * 16, xq, xs,
+                       tid, NC, f.err);
     named_bar(1, NC);
     good = consume_phase<FmtD, MODE_DOWN>(f.dn, ring, s_idx, s_w, xq, xs, part, db, de, it, tid);
     if (tid == 0) {

@@ -469,10 +469,9 @@ qmoe_status qmv(int qtype, const void* W, int64_t rows, int64_t cols, const floa
         return fail(QMOE_ERR_INVALID_ARGUMENT,
                     "qmv: cols=%lld is not a whole number of %s blocks (%d elements)",
                     (long long)cols, qname(qtype), block_elems(qtype));
-    if (qtype == QT_F32 ? (cols % 4 != 0) : (cols % 256 != 0))
-        return fail(QMOE_ERR_UNSUPPORTED,
-                    "qmv: cols=%lld must be a multiple of %d for %s on this path",
-                    (long long)cols, qtype == QT_F32 ? 4 : 256, qname(qtype));
+    if (qtype == QT_F32 && cols % 4 != 0)
+        return fail(QMOE_ERR_UNSUPPORTED, "qmv: cols=%lld must be a multiple of 4 for F32",
+                    (long long)cols);
     if (cols > MAX_K)
         return fail(QMOE_ERR_UNSUPPORTED, "qmv: cols=%lld exceeds %lld", (long long)cols,
                     (long long)MAX_K);
@@ -488,7 +487,9 @@ qmoe_status qmv(int qtype, const void* W, int64_t rows, int64_t cols, const floa
         return run_f32_gemv(static_cast<const float*>(W), x, y, rows, cols, st);
     StreamParams p = {};
     p.units = rows;
-    p.nb_seg = static_cast<int>(cols / 256);
+    // Q8_0 / Q4_0 rows may end in a partial group of 32-element blocks
+    p.nb_seg = static_cast<int>((cols + 255) / 256);
+    p.tail = static_cast<int>((cols % 256) / 32);
     p.n_kseg = 1;
     p.W0 = static_cast<const uint8_t*>(W);
     p.rb0 = row_bytes_of(qtype, cols);

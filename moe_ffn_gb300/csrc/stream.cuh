@@ -48,7 +48,8 @@ struct StreamParams {
     int64_t units;       // output units: rows (QMV, DOWN) or gate/up row pairs (GATEUP)
     int64_t uq;          // units per CTA, rounded down (units / grid)
     int ur;              // CTAs that take one more unit (units % grid)
-    int nb_seg;          // 256-element groups per k-segment
+    int nb_seg;          // 256-element groups per k-segment (the last may be partial)
+    int tail;            // Q8_0/Q4_0 only: 32-element blocks of a partial last group (0: none)
     int n_kseg;          // k-segments: 1, or top_k for the MoE down product
     int chunk_ks;        // whole k-segments per chunk (when n_sbc == 1)
     int chunk_sb;        // groups per k-segment per chunk
@@ -81,6 +82,13 @@ template <int MODE> struct ModeGeom {
     static constexpr int TU = (MODE == MODE_GATEUP) ? ROWS / 2 : ROWS;  // units per tile
     static constexpr int WK = NCW;                         // warps along K
 };
+
+// Bytes of one k-segment of a row: nb_seg groups, the last one short by the
+// blocks a partial group lacks (Q8_0/Q4_0 rows of 32-element blocks).
+template <class Fmt>
+__host__ __device__ inline int seg_bytes(const StreamParams& p) {
+    return p.nb_seg * Fmt::SBB - (p.tail ? (8 - p.tail) * (Fmt::SBB / 8) : 0);
+}
 
 // The x table of one 256-element group: the 64 pre-scaled activations x' of
 // each quarter lane (float4 [16][4]), and beside it in the xs region 16 sums
@@ -219,8 +227,8 @@ __device__ inline float rms_inverse(const float* __restrict__ h, int n, float ep
 }
 
 template <class Fmt, int UNR = 4>
-__device__ inline void build_xprime(const float* __restrict__ x, int ngroups, float* xq,
-                                    float* xs, int tid, int nthreads, DevCtl* err,
+__device__ inline void build_xprime(const float* __restrict__ x, int ngroups, int n16_valid,
+                                    float* xq, float* xs, int tid, int nthreads, DevCtl* err,
                                     const float* __restrict__ nw = nullptr, float inv = 1.f,
                                     const float* inv_tok = nullptr, int tok_n16 = 0,
                                     const float* __restrict__ rrow = nullptr,
@@ -238,6 +246,8 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
     // slot four consecutive elements), each element scaled for its field's
     // bit position.  A block whose largest |x| is 2^106 or more is outside
     // the range and is flagged (DEV_X_RANGE).
+    // Only the first n16_valid chunks of x exist (a row whose last group is
+    // partial); the table holds zeros past them.
     // With nw, the table is of the normed input x_j * inv * nw_j (ffn_norm).
     // With inv_tok, x holds several tokens of tok_n16 chunks each, token t
     // normed with inv_tok[t] (nw applies per token).  UNR chunks per thread
@@ -262,7 +272,7 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, fl
         for (int u = 0; u < UNR; ++u) {
             if (wbase + u * nthreads >= n16) break;  // warp-uniform: no lane of the warp has work
             const int c = base + u * nthreads;
-            if (c < n16) {
+            if (c < n16_valid) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[u][k] = __ldcg(x4 + 4 * c + k);
                 int cw = c;
@@ -521,10 +531,12 @@ __device__ __forceinline__ uint32_t chunk_copy(const StreamParams& p, const int3
     const uint8_t* a = row_addr<MODE>(p, s_idx, u0, s0, uend, r, cd.ks0 + pk);
     if (!a) return 0u;
     const uintptr_t sa = reinterpret_cast<uintptr_t>(a) + static_cast<uintptr_t>(cd.b0) * Fmt::SBB;
+    // never past the row's end (a partial last group is shorter)
+    const int seg = seg_bytes<Fmt>(p), want = cd.nbp * Fmt::SBB, left = seg - cd.b0 * Fmt::SBB;
+    const uintptr_t n = static_cast<uintptr_t>(want < left ? want : left);
     src = sa & ~uintptr_t(15);
     dst = r * p.slot_stride + pk * p.piece_stride;
-    return static_cast<uint32_t>(
-        ((sa + static_cast<uintptr_t>(cd.nbp) * Fmt::SBB + 15) & ~uintptr_t(15)) - src);
+    return static_cast<uint32_t>(((sa + n + 15) & ~uintptr_t(15)) - src);
 }
 
 // After a wait of the producer gave up: wait (bounded) until the copies of
@@ -644,6 +656,7 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
                 const int ks = cd.ks0 + pk, b = cd.b0 + bb;
                 const int gidx = ks * p.nb_seg + b;
                 const float* xsg = xs + gidx * XS_GROUP_FLOATS;
+                const int nblk = (p.tail && b == p.nb_seg - 1) ? p.tail : 8;
                 const uint32_t ksoff =
                     (MODE == MODE_DOWN && p.moe)
                         ? static_cast<uint32_t>(s_idx[ks]) * static_cast<uint32_t>(p.es0)
@@ -656,7 +669,7 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
                     const int delta = static_cast<int>((rowlo[rr] + ksoff + b0off) & 15u);
                     sbp[rr] = st + rowoff[rr] + pk * p.piece_stride + delta + bb * Fmt::SBB;
                 }
-                Fmt::template dotR<R>(sbp, q, xq4 + gidx * 64 + q, xsg, xsg + 16, acc);
+                Fmt::template dotR<R>(sbp, q, xq4 + gidx * 64 + q, xsg, xsg + 16, nblk, acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ring.empty[s]);
@@ -710,11 +723,12 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
 
 // QMV launches are bounded to two CTAs per SM (96 registers with nine warps
 // per CTA: the register file is split between the four sub-partitions), so
-// the next launch's CTAs can stream their weights beside this one.  Q6_K
-// needs more registers than that without spilling and keeps one per SM.
+// the next launch's CTAs can stream their weights beside this one.  Q6_K and
+// Q8_0 need more registers than that without spilling (and a 4096-wide
+// Q8_0 tile does not fit two per SM anyway): they keep one per SM.
 template <class Fmt, int MODE>
 constexpr int stream_min_blocks() {
-    return (MODE == MODE_QMV && Fmt::SBB != 210) ? 2 : 1;
+    return (MODE == MODE_QMV && Fmt::SBB != 210 && Fmt::SBB != 272) ? 2 : 1;
 }
 
 template <class Fmt, int MODE>
@@ -777,7 +791,9 @@ __global__ void __launch_bounds__(NTHREADS, (stream_min_blocks<Fmt, MODE>())) st
         pdl_wait();
         pdl_trigger();
     }
-    build_xprime<Fmt>(p.x, p.nb_seg * p.n_kseg, xq, xs, tid, NCW * 32, p.err);
+    build_xprime<Fmt>(p.x, p.nb_seg * p.n_kseg,
+                      p.tail ? (p.nb_seg - 1) * 16 + 2 * p.tail : p.nb_seg * p.n_kseg * 16, xq, xs,
+                      tid, NCW * 32, p.err);
     named_bar(1, NCW * 32);
     if (!p.moe) named_bar(2, NTHREADS);  // the stage barriers are initialised
     consume_phase<Fmt, MODE>(p, ring, s_idx, s_w, xq, xs, part, ubeg, uend, it, tid);
@@ -795,7 +811,10 @@ inline bool plan_chunks(StreamParams& p, int budget, int rows = ModeGeom<MODE>::
     using G = ModeGeom<MODE>;
     if (MODE != MODE_QMV || rows > G::ROWS || rows < 1) rows = G::ROWS;
     if (budget < rows * (Fmt::SBB + 31)) return false;
-    const int seg_full = p.nb_seg * Fmt::SBB;
+    const int seg_full = seg_bytes<Fmt>(p);
+    // a partial last group is read as a whole one: the bytes past the row
+    // end are stale shared memory, masked off by the consumer
+    const int tail_slack = p.tail ? Fmt::SBB : 0;
     // Whole k-segments fit: runs of consecutive rows, one bulk copy each.
     // A k-segment region holds the tile's rows at their global stride plus
     // slack for up to four run starts (32 bytes apart), a 16-byte phase and
@@ -803,7 +822,7 @@ inline bool plan_chunks(StreamParams& p, int budget, int rows = ModeGeom<MODE>::
     // Rows of 2 KB and more stream at the full rate as separate copies, so
     // formats whose loads would conflict at the global stride keep padded
     // per-row slots for them.
-    const int run_piece = align_up(rows * seg_full, 16) + 144;
+    const int run_piece = align_up(rows * seg_full, 16) + 144 + tail_slack;
     if (run_piece <= budget && (Fmt::RUNS_OK || seg_full < 2048)) {
         p.runs = 1;
         p.n_sbc = 1;

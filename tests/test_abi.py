@@ -71,7 +71,8 @@ FAKE = 1 << 20  # a 16-byte-aligned non-null address, never dereferenced
     ((qm.Q4_K, None, 4, 256, FAKE, FAKE), qm.ERR_INVALID_ARGUMENT),
     ((qm.Q4_K, FAKE, 0, 256, FAKE, FAKE), qm.ERR_INVALID_ARGUMENT),
     ((qm.Q4_K, FAKE, 4, 100, FAKE, FAKE), qm.ERR_INVALID_ARGUMENT),
-    ((qm.Q8_0, FAKE, 4, 96, FAKE, FAKE), qm.ERR_UNSUPPORTED),
+    ((qm.Q4_K, FAKE, 4, 96, FAKE, FAKE), qm.ERR_INVALID_ARGUMENT),
+    ((qm.F32, FAKE, 4, 6, FAKE, FAKE), qm.ERR_UNSUPPORTED),
     ((qm.Q4_K, FAKE + 4, 4, 256, FAKE, FAKE), qm.ERR_INVALID_ARGUMENT),
     ((17, FAKE, 4, 256, FAKE, FAKE), qm.ERR_UNSUPPORTED),
     ((qm.Q4_K, FAKE, 4, 1 << 20, FAKE, FAKE), qm.ERR_UNSUPPORTED),

@@ -374,3 +374,41 @@ def test_moe_non_finite_activation(qm, orc, shp, bad):
     assert idx[tb].tolist() == list(range(K))
     assert np.all(np.isnan(w[tb])) and np.all(np.isnan(out.reshape(T, -1)[tb]))
     assert check_moe(out, idx, w, ref) <= max(1, T // 20)
+
+
+# ------------------------------------- Q8_0 / Q4_0 widths of 32-element blocks
+@pytest.mark.parametrize("qt", [synth.Q8_0, synth.Q4_0], ids=lambda q: QNAME[q])
+@pytest.mark.parametrize("rows,cols", [(5, 96), (37, 896), (300, 4128), (64, 32), (17, 288),
+                                       (153, 4064), (9, 32736)])
+def test_qmv_widths_of_32(qm, orc, qt, rows, cols):
+    """cols a multiple of 32 but not of 256 (block_bytes_per_row on
+    "ferrox-core 0.16.0 — weight_matrix.rs" needs only whole 32-element
+    blocks): the last 256-element group of each row is partial, and rows of
+    an odd number of blocks sit at 2-byte-aligned offsets."""
+    g = synth.rng(2000 + qt * 11 + cols)
+    W = synth.quant_matrix(g, qt, rows, cols, nan_row=rows // 2 if rows > 2 else None)
+    x = synth.normal(g, cols)
+    y = gpu_qmv(qm, qt, W, rows, cols, x)
+    ref, sabs = orc.matvec(qt, W, rows, cols, x, with_sabs=True)
+    check_gemv(y, ref, sabs, f"qmv {QNAME[qt]} {rows}x{cols}")
+    assert qm.device_status() == qm.OK
+
+
+# ------------------------------------------------------ lm_head-sized GEMVs
+@pytest.mark.parametrize("qt", [synth.F32, synth.Q6_K, synth.Q8_0], ids=lambda q: QNAME[q])
+def test_qmv_lm_head_size(qm, orc, qt):
+    """vocab 151,936 x hidden 2048 (a Qwen3-sized output projection): every
+    row checked.  The pages keep the F32 router and the lm_head GEMV on the
+    host ("ferrox-core 0.16.0 — weight_matrix.rs", apply_gpu); here they run
+    on the device through the same entry point."""
+    g = synth.rng(151936 + qt)
+    rows, cols = 151936, 2048
+    if qt == synth.F32:
+        W = synth.normal(g, (rows, cols), 0.02)
+        Wb = W.view(np.uint8)
+    else:
+        W = Wb = synth.quant_matrix(g, qt, rows, cols, nan_row=7)
+    x = synth.normal(g, cols)
+    y = gpu_qmv(qm, qt, W, rows, cols, x)
+    ref, sabs = orc.matvec(orc.F32 if qt == synth.F32 else qt, Wb, rows, cols, x, with_sabs=True)
+    check_gemv(y, ref, sabs, f"lm_head {QNAME[qt]}")
