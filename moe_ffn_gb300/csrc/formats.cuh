@@ -169,6 +169,8 @@ struct FmtQ4K {
         // bit offsets {0, 8, 16, 0, 4, 12, 20, 0} by i % 8, one byte each
         return static_cast<int>((0x00140C0400100800ull >> (8 * (i & 7))) & 0xFFu);
     }
+    // pos depends on i % 8 (not only i % 4): the x table's scales use it
+    static constexpr bool POS8 = true;
     // 6-bit (sc, m) of pairs 2q and 2q+1 — the unpacking of
     // ferrox_q4_k_scale_min, four pairs per 32-bit word: pairs 0..3 are the
     // low 6 bits of bytes 0..3 (sc) and 4..7 (m); pairs 4..7 join the low /
@@ -253,6 +255,7 @@ struct FmtQ5K {
         // bit offsets {0, 8, 16, 0} by i % 4
         return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
     }
+    static constexpr bool POS8 = false;
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
@@ -336,6 +339,7 @@ struct FmtQ6K {
         // bit offsets {0, 8, 16, 0} by i % 4
         return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
     }
+    static constexpr bool POS8 = false;
     // Words [4k, 4k+4) of the 32-byte window (lo, hi), J words plus sh bits in.
     template <int J>
     __device__ __forceinline__ static void window4(const uint4& lo, const uint4& hi, uint32_t sh,
@@ -488,6 +492,7 @@ struct FmtQ80 {
         // bit offsets {0, 8, 16, 0} by i % 4
         return static_cast<int>((0x00100800u >> (8 * (i & 3))) & 0xFFu);
     }
+    static constexpr bool POS8 = false;
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
@@ -552,6 +557,7 @@ struct FmtQ40 {
         return 4 * i4 + (blk >> 1);
     }
     __host__ __device__ static int pos(int q, int i) { return FmtQ4K::pos(q, i); }
+    static constexpr bool POS8 = true;
     template <int R>
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,

@@ -347,15 +347,20 @@ __device__ inline void build_xprime(const float* __restrict__ x, int ngroups, in
                 const int g = c >> 4;
                 xs[g * XS_GROUP_FLOATS + (c & 15)] = s;
                 if ((c & 1) == 0) xs[g * XS_GROUP_FLOATS + 16 + ((c & 15) >> 1)] = pow2f(21 + E);
+                // 2^(128 - E - pos) for the granule's four positions, which
+                // are those of element index i % 8 (formats.cuh): {0, 8, 16,
+                // 0} for i % 8 < 4, and {4, 12, 20, 0} above it where POS8
+                const float base = pow2f(128 - E);
+                const float m0 = base, m1 = base * 0x1p-8f, m2 = base * 0x1p-16f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int slot = Fmt::xslot(4 * (c & 15) + k);
-                    const int q = slot & 3, i = 4 * (slot >> 2);
+                    const bool odd = Fmt::POS8 && ((slot >> 2) & 1);
                     float4 o;
-                    o.x = v[u][k].x * pow2f(128 - E - Fmt::pos(q, i));
-                    o.y = v[u][k].y * pow2f(128 - E - Fmt::pos(q, i + 1));
-                    o.z = v[u][k].z * pow2f(128 - E - Fmt::pos(q, i + 2));
-                    o.w = v[u][k].w * pow2f(128 - E - Fmt::pos(q, i + 3));
+                    o.x = v[u][k].x * (odd ? base * 0x1p-4f : m0);
+                    o.y = v[u][k].y * (odd ? base * 0x1p-12f : m1);
+                    o.z = v[u][k].z * (odd ? base * 0x1p-20f : m2);
+                    o.w = v[u][k].w * base;
                     xq4[g * 64 + slot] = o;
                 }
             }

@@ -254,6 +254,30 @@ def test_moe_decode_workload(qm, orc):
     assert check_moe(out, idx, w, ref) == 0
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_moe_input_is_residual(qm, orc, T):
+    """x and residual the same buffer: every token reads its input before any
+    product is added to it (the clusters of the single-token kernel do not
+    wait for each other, so such a call takes the other kernels)."""
+    import torch
+    shp = dict(synth.MOE_DECODE, n_tokens=T)
+    inp = synth.moe_inputs(44 + T, **shp)
+    inp = dict(inp, x=inp["residual"].copy())
+    K = shp["top_k"]
+    s = qm.moe_shape(shp["hidden"], shp["expert_dim"], shp["num_experts"], K, T, shp["gate"],
+                     shp["up"], shp["down"])
+    res = _dev(inp["residual"])
+    idx = torch.full((T, K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, K), device="cuda")
+    ws = torch.zeros(qm.moe_ffn_workspace_size(s), dtype=torch.uint8, device="cuda")
+    qm.moe_ffn(_dev(inp["router"]), _dev(inp["gate"]), _dev(inp["up"]), _dev(inp["down"]), s,
+               res, res, idx, w, ws)
+    torch.cuda.synchronize()
+    assert qm.device_status() == qm.OK
+    ref = oracle_moe(orc, inp, shp)
+    assert check_moe(res.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), ref) == 0
+
+
 def test_moe_prefill_workload_sampled(qm, orc):
     """OLMoE-shaped, 512 tokens: every token's routing checked exactly;
     residuals of 12 sampled tokens checked against the oracle."""
