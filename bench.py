@@ -556,14 +556,28 @@ def _oracle_sweeps(seconds):
     return n, time.perf_counter() - t0
 
 
+# Arm "CPU part" numbers (implementer 0x41) of the cores these hosts carry
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+             "0xd49": "Arm Neoverse N2", "0xd8f": "Arm Neoverse V3"}
+
+
 def cpu_model():
+    """The host CPU's name: x86 'model name', or an Arm core's part number
+    with its name when known (e.g. 0xd4f, Neoverse V2 as in Grace)."""
+    part = None
     try:
         for line in open("/proc/cpuinfo"):
             k, _, v = line.partition(":")
-            if k.strip() in ("model name", "Model name", "CPU part"):
-                return v.strip()
+            k, v = k.strip(), v.strip()
+            if k in ("model name", "Model name"):
+                return v
+            if k == "CPU part" and part is None:
+                part = v
     except OSError:
         pass
+    if part:
+        name = ARM_PARTS.get(part.lower())
+        return f"{name} (CPU part {part})" if name else f"Arm CPU part {part}"
     import platform
     return platform.processor() or platform.machine()
 

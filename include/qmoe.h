@@ -199,9 +199,20 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  * Execution: for T >= 32 tokens with Q4_K gate/up and Q6_K down stacks, the
  * tokens are grouped by expert and the expert products run on the tensor
  * cores, whose operands are rounded once: gate/up weights and x (scaled per
- * token by a power of two) to f16, down weights and the activations to
- * tf32, so each product carries at most 2 * 2^-11 relative error, inside the
- * bound above.  A single token runs one cooperative kernel (one CTA per SM):
+ * token by 2^s so that its largest |x| lies in [2^14, 2^15)) to f16, down
+ * weights and the activations to tf32 (round to nearest).  A product of
+ * operands in f16's normal range, and every down product, carries at most
+ * 2 * 2^-11 relative error, inside the bound above.  f16's range adds two
+ * absolute terms, outside that bound: an element of x below 2^-28 of its
+ * token's largest |x| is rounded to f16's subnormal spacing (error at most
+ * 2^-39 * max|x| per element), and so is a decoded gate/up weight of
+ * magnitude below 2^-14 (error at most 2^-25 per weight).  Each is far
+ * below the bound unless a token's large activations meet zero weights and
+ * its other activations are more than 2^28 times smaller, or a row's
+ * decoded weights are nearly all below 2^-14; the single-token and
+ * small-batch paths (f32 throughout) have neither term.  A decoded gate/up
+ * weight beyond f16's range is flagged (QMOE_ERR_UNSUPPORTED from
+ * qmoe_device_status).  A single token runs one cooperative kernel (one CTA per SM):
  * router GEMV, a grid barrier, routing in every CTA, the routed gate/up rows
  * and then the down rows streamed through one pipeline, a second grid barrier
  * before the down products.  2..31 tokens run in cooperative launches of up

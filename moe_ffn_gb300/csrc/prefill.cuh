@@ -17,8 +17,12 @@
 // Operand precision: gate/up weights are decoded exactly in f32 and rounded
 // once to f16; x is scaled per token by a power of two into f16's range and
 // rounded once.  Down weights and the activations are rounded to tf32 (round
-// to nearest).  Each product then carries at most 2 * 2^-11 relative error,
-// inside the 1e-3 * sum|w x| bound.  The down product's contributions of the
+// to nearest).  A product of operands in f16's normal range (and every down
+// product) then carries at most 2 * 2^-11 relative error, inside the
+// 1e-3 * sum|w x| bound; elements of x below 2^-28 of their token's largest
+// |x|, and decoded gate/up weights below 2^-14, fall in f16's subnormal
+// range and are rounded to its spacing (an absolute error, stated in the
+// library header).  The down product's contributions of the
 // k experts are added to the residual with atomics, so their summation order
 // varies from run to run (within the same bound).
 #pragma once
