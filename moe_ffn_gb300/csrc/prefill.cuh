@@ -10,9 +10,12 @@
 //                      pairs appended to each expert's list, x copied to f16
 //                      with a power-of-two scale
 //   pf_gateup_kernel   per (expert, 128 features): D_g = G X^T, D_u = U X^T
-//                      (f16 x f16 -> f32); a[pair][f] = w * silu(g) * u
+//                      (f16 x f16 -> f32); a = w * silu(g) * u, rounded to
+//                      tf32, into row (expert's first row + list position)
+//                      of an expert-major activation array
 //   pf_down_kernel     per (expert, 128 rows of H): D = Dn A^T (tf32 x tf32
-//                      -> f32); residual[t][i] += D  (atomic adds)
+//                      -> f32), A's tiles loaded by 2-D tensor copies from
+//                      that array; residual[t][i] += D  (atomic adds)
 //
 // Operand precision: gate/up weights are decoded exactly in f32 and rounded
 // once to f16; x is scaled per token by a power of two into f16's range and
@@ -226,7 +229,8 @@ struct PfParams {
     const __half* X16;
     const float* xinv;
     const float* tw;
-    float* a;         // [T*K][F] activations
+    float* a;         // [T*K][F] activations, expert-major (rows of expert e from
+                      // the pairs routed to experts 0..e-1 on), tf32-rounded
     float* residual;  // [T][H]
     DevCtl* err;
 };
@@ -259,6 +263,16 @@ __device__ __forceinline__ float to_tf32(float v) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
     return __uint_as_float(r);
+}
+
+// First row of expert e in the expert-major activation array: the number
+// of (token, slot) pairs routed to experts 0..e-1.  By a whole warp.
+__device__ __forceinline__ int expert_row0(const int32_t* __restrict__ cnt, int e, int lane) {
+    int n = 0;
+    for (int i = lane; i < e; i += 32) n += __ldcg(cnt + i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    return n;
 }
 
 // --------------------------------------------------------- gate / up (f16)
@@ -296,7 +310,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     int64_t* meta_tok = reinterpret_cast<int64_t*>(bars + 12);          // [2][PF_NP]
     float* meta_xinv = reinterpret_cast<float*>(meta_tok + 2 * PF_NP);  // [2][PF_NP]
     float* meta_w = meta_xinv + 2 * PF_NP;                              // [2][PF_NP]
-    int32_t* meta_pair = reinterpret_cast<int32_t*>(meta_w + 2 * PF_NP);  // [2][PF_NP]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int FT = p.F / 128;              // feature tiles per expert
@@ -418,6 +431,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (n == 0) continue;
         const int passes = (n + PF_NP - 1) / PF_NP;
         const int32_t* lst = p.list + static_cast<int64_t>(e) * p.T;
+        const int row0 = expert_row0(p.cnt, e, lane);
         for (int pass = 0; pass < passes; ++pass, ++acc_round) {
             const int nt = min(PF_NP, n - pass * PF_NP);
             const int np = (nt + 15) & ~15;
@@ -425,11 +439,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             int64_t* mt_tok = meta_tok + (acc_round & 1) * PF_NP;
             float* mt_xinv = meta_xinv + (acc_round & 1) * PF_NP;
             float* mt_w = meta_w + (acc_round & 1) * PF_NP;
-            int32_t* mt_pair = meta_pair + (acc_round & 1) * PF_NP;
             if (wt < nt) {
                 const int pair = __ldcg(lst + pass * PF_NP + wt);
                 const int t = pair / p.K;
-                mt_pair[wt] = pair;
                 mt_tok[wt] = static_cast<int64_t>(t) * p.H;
                 mt_xinv[wt] = __ldcg(p.xinv + t);
                 mt_w[wt] = __ldcg(p.tw + pair);
@@ -521,7 +533,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ab_full[s]);
             }
-            // ---- epilogue: a[pair][f] = w * silu(g) * u
+            // ---- epilogue: a = w * silu(g) * u, tf32-rounded (the down
+            // product's operand), at the pair's row of the expert-major array
             if (!mbar_wait_bounded(acc_full, acc_round & 1, p.err, DEV_PF_TIMEOUT)) goto done;
             umma::fence_after_sync();
             const int lq = warp & 3;               // TMEM lane quarter of this warp
@@ -539,8 +552,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     if (j < nt && j < c1) {
                         const float xi = mt_xinv[j];
                         const float gv = g[i] * xi, uv = u[i] * xi;
-                        p.a[static_cast<int64_t>(mt_pair[j]) * p.F + f] =
-                            mt_w[j] * ((gv / (1.0f + expf(-gv))) * uv);
+                        p.a[static_cast<int64_t>(row0 + pass * PF_NP + j) * p.F + f] =
+                            to_tf32(mt_w[j] * ((gv / (1.0f + expf(-gv))) * uv));
                     }
                 }
             }
@@ -562,13 +575,20 @@ done:
 // the raw Q6_K rows of one (expert, 128-row) tile, all of F, as they lie in
 // memory (the 128 rows are consecutive, so one bulk copy moves them);
 // barriers; TMEM address.  F <= PF_DN_MAX_F.
+// B (the activations of a pass's pairs, columns kc*32 .. +32) is one 2-D
+// tensor copy of 128 rows x 128 bytes with the 128-byte swizzle the MMA
+// reads, from the expert-major array pf_gateup wrote already rounded to
+// tf32: rows past the expert's pairs (the next expert's, or zeros past the
+// array) land in MMA columns that are never read back.  A stage is full when
+// the eight decode warps have arrived and the copy's bytes have landed.
 constexpr int PF_DN_MAX_F = 1280;
 constexpr int DN_RAW_MAX = 128 * (PF_DN_MAX_F / 256) * 210 + 32;  // 134,432
 constexpr int DN_TILE = 128 * 128;                  // 16,384
 constexpr int DN_AB_STAGE = 2 * DN_TILE;            // 32,768
 constexpr int DN_SMEM = 1024 + 2 * DN_AB_STAGE + DN_RAW_MAX + PF_META;
 
-__global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p) {
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    pf_down_kernel(const PfParams p, const __grid_constant__ CUtensorMap tm_act) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -583,7 +603,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
     uint64_t* acc_empty = bars + 9;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
     int64_t* meta_res = reinterpret_cast<int64_t*>(bars + 12);   // [2][PF_NP] residual row offset
-    int64_t* meta_act = meta_res + 2 * PF_NP;                    // [2][PF_NP] activation row offset
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int MT = p.H / 128;              // row tiles per expert
@@ -594,7 +613,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
         for (int i = 0; i < 2; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], PF_WORKERS);
-            mbar_init(&ab_full[i], PF_WORKERS);
+            mbar_init(&ab_full[i], PF_WORKERS + 1);  // + the producer's B copy
             mbar_init(&ab_empty[i], 1);
         }
         mbar_init(acc_full, 1);
@@ -609,19 +628,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
     pdl_trigger();
 
     if (warp == 0) {
-        // one bulk copy per tile: the item's 128 consecutive rows, all of F
+        // one bulk copy per tile: the item's 128 consecutive rows, all of F;
+        // then, per pass and 32-column chunk, the B tile's tensor copy
         const uint64_t pol = policy_evict_first();
+        const uint64_t pol_act = policy_evict_last();  // re-read by the expert's 16 row tiles
         const int64_t tile_bytes = 128 * p.rb;
-        int rit = 0;
-        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int KC = p.F / 32;
+        int rit = 0, kit = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < items; item += gridDim.x) {
             const int e = item / MT, mt = item % MT;
             const int n = __ldcg(p.cnt + e);
             if (n == 0) continue;
+            const int row0 = expert_row0(p.cnt, e, lane);
             if (rit > 0 &&
                 !mbar_wait_bounded(&raw_empty[0], (rit - 1) & 1, p.err, DEV_PF_TIMEOUT)) {
-                // the previous copy still completes; wait for it, then leave
-                mbar_wait_bounded(&raw_full[0], (rit - 1) & 1, p.err, DEV_PF_TIMEOUT);
-                return;
+                ok = false;
+                break;
             }
             if (lane == 0) {
                 const uintptr_t src = reinterpret_cast<uintptr_t>(
@@ -634,9 +657,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
             }
             __syncwarp();
             ++rit;
+            const int passes = (n + PF_NP - 1) / PF_NP;
+            for (int pass = 0; ok && pass < passes; ++pass) {
+                for (int kc = 0; kc < KC; ++kc, ++kit) {
+                    const int s = kit & 1, round = kit >> 1;
+                    if (round > 0 &&
+                        !mbar_wait_bounded(&ab_empty[s], (round - 1) & 1, p.err, DEV_PF_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&ab_full[s], DN_TILE);
+                        tma_load_2d(ab + s * DN_AB_STAGE + DN_TILE, &tm_act, kc * 32,
+                                    row0 + pass * PF_NP, &ab_full[s], pol_act);
+                    }
+                    __syncwarp();
+                }
+            }
         }
-        // never leave with a copy in flight
+        // never leave with a copy in flight: the last weight tile, the last
+        // (up to two) B tiles (their stages complete once the decode warps
+        // arrive too; every wait is bounded)
         if (rit > 0) mbar_wait_bounded(&raw_full[0], (rit - 1) & 1, p.err, DEV_PF_TIMEOUT);
+        for (int k = kit - 2; k < kit; ++k)
+            if (k >= 0) mbar_wait_bounded(&ab_full[k & 1], (k >> 1) & 1, p.err, DEV_PF_TIMEOUT);
         return;
     }
     if (warp == 1) {
@@ -702,41 +746,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
             const int nt = min(PF_NP, n - pass * PF_NP);
             const int np = (nt + 15) & ~15;
             int64_t* mt_res = meta_res + (acc_round & 1) * PF_NP;
-            int64_t* mt_act = meta_act + (acc_round & 1) * PF_NP;
             if (wt < nt) {
                 const int pair = __ldcg(lst + pass * PF_NP + wt);
                 mt_res[wt] = static_cast<int64_t>(pair / p.K) * p.H;
-                mt_act[wt] = static_cast<int64_t>(pair) * p.F;
             }
             named_bar(2, PF_WORKERS * 32);
-            // B: activations a[pair][kc*32 .. +32].  Each chunk's loads are
-            // issued one chunk ahead, so their L2 latency hides behind the
-            // previous chunk's A decode; rounded to tf32 when stored.
-            constexpr int NBV = PF_NP * 8 / 256;
             const int KC = p.F / 32;
-            float4 bv[NBV];
-#pragma unroll
-            for (int k = 0; k < NBV; ++k) {
-                const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
-                bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < nt)
-                    bv[k] = __ldcg(reinterpret_cast<const float4*>(p.a + mt_act[j] + ch * 4));
-            }
             for (int kc = 0; kc < KC; ++kc, ++kit) {
                 const int s = kit & 1, round = kit >> 1;
                 if (round > 0 &&
                     !mbar_wait_bounded(&ab_empty[s], (round - 1) & 1, p.err, DEV_PF_TIMEOUT))
                     goto done;
                 uint8_t* st = ab + s * DN_AB_STAGE;
-                float4 bn[NBV];  // chunk kc + 1
-#pragma unroll
-                for (int k = 0; k < NBV; ++k) {
-                    const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
-                    bn[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (j < nt && kc + 1 < KC)
-                        bn[k] = __ldcg(reinterpret_cast<const float4*>(p.a + mt_act[j] +
-                                                                       (kc + 1) * 32 + ch * 4));
-                }
                 // A: row r = wt/2, 16 values (half hh) of the 32-element chunk
                 const int sbk = kc & 7;            // chunk within the super-block
                 {
@@ -773,19 +794,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_down_kernel(const PfParams p
                                         to_tf32(fmaf(byte_as_half_plus(v[c], SEL_B2), A, C)),
                                         to_tf32(fmaf(byte_as_half_plus(v[c], SEL_B3), A, C)));
                     }
-                }
-#pragma unroll
-                for (int k = 0; k < NBV; ++k) {
-                    const int c = wt + 256 * k, j = c >> 3, ch = c & 7;
-                    if (j < np) {
-                        float4 w = bv[k];
-                        w.x = to_tf32(w.x);
-                        w.y = to_tf32(w.y);
-                        w.z = to_tf32(w.z);
-                        w.w = to_tf32(w.w);
-                        *reinterpret_cast<float4*>(st + DN_TILE + umma::sw128_offset(j, ch * 16)) = w;
-                    }
-                    bv[k] = bn[k];
                 }
                 if (pass == passes - 1 && kc == KC - 1) {
                     // the tile's last chunk is decoded: its rows may be replaced

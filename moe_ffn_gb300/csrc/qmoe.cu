@@ -723,6 +723,25 @@ static qmoe_status rows_map(CUtensorMap* m, const void* base, int64_t row_bytes,
     return QMOE_OK;
 }
 
+// A [rows][cols] f32 matrix as a 2-D tensor map with boxes of box_cols x
+// box_rows, 128-byte swizzled (box_cols * 4 == 128: the MMA's K-major
+// operand layout).  cols * 4 and the base must be multiples of 16 bytes.
+static qmoe_status f32_swizzled_map(CUtensorMap* m, const float* base, int64_t cols, int64_t rows,
+                                    uint32_t box_cols, uint32_t box_rows) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return fail(QMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                          const_cast<float*>(base), dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QMOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return QMOE_OK;
+}
+
 static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
                                const void* up_stack, const void* down_stack,
                                const qmoe_moe_shape& s, const float* x, float* residual,
@@ -788,8 +807,14 @@ static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
     pd.rb = row_bytes_of(QT_Q6_K, F);
     pd.es = pd.rb * H;
     const int items_dn = E * (H / 128);
+    // the activations, expert-major [T*K][F], as the down product's B tiles:
+    // 32 columns (one 128-byte swizzle row) x PF_NP pairs per copy
+    CUtensorMap tm_act;
+    if (qmoe_status r = f32_swizzled_map(&tm_act, a, F, static_cast<int64_t>(T) * K, 32,
+                                         pf::PF_NP))
+        return r;
     e = launch_pdl(pf::pf_down_kernel, dim3(items_dn < d.sms ? items_dn : d.sms),
-                   dim3(pf::PF_THREADS), static_cast<size_t>(pf::DN_SMEM), st, pd);
+                   dim3(pf::PF_THREADS), static_cast<size_t>(pf::DN_SMEM), st, pd, tm_act);
     if (e != cudaSuccess) return cuda_fail(e, "pf_down launch");
     return QMOE_OK;
 }
