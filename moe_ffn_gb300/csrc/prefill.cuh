@@ -45,19 +45,34 @@ enum : unsigned { DEV_PF_TIMEOUT = 16, DEV_PF_RANGE = 17 };
 // ------------------------------------------------------------------ router
 // CTA = 8 tokens x 32 experts (one thread each; a warp is one token).  x and
 // R are staged through shared memory 256 columns at a time (R rows padded to
-// 260 floats so a warp's 32 rows fall in distinct banks).  The sum runs in
-// three levels (16 products, 16 of those, the rest) so its f32 error stays
-// near 40 ulp of sum |R x| whatever H is.
+// 260 floats so a warp's 32 rows fall in distinct banks), two stages deep:
+// the 16-byte asynchronous copies of chunk c + 1 are in flight while chunk c
+// is summed.  The sum runs in three levels (16 products, 16 of those, the
+// rest) so its f32 error stays near 40 ulp of sum |R x| whatever H is.
 constexpr int RT_TOK = 8;   // tokens per CTA (one per warp)
 constexpr int RT_KC = 256;  // columns per staged chunk
 constexpr int RT_LD = 260;  // padded row stride (floats)
+constexpr int RT_STAGE = RT_TOK * RT_KC + 32 * RT_LD;  // floats per stage
+constexpr int RT_SMEM = 2 * RT_STAGE * 4;              // 82,944 bytes
+
+__device__ __forceinline__ void cp_async16_cg(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __global__ void __launch_bounds__(256) pf_router_kernel(const float* __restrict__ R,
                                                         const float* __restrict__ X, int T,
                                                         int H, int E, float* __restrict__ logits,
                                                         int32_t* __restrict__ cnt) {
-    __shared__ __align__(16) float sx[RT_TOK][RT_KC];
-    __shared__ __align__(16) float sr[32][RT_LD];
+    extern __shared__ __align__(16) float rt_smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * RT_TOK, e0 = blockIdx.y * 32;
     const int t = t0 + warp, e = e0 + lane;
@@ -65,26 +80,41 @@ __global__ void __launch_bounds__(256) pf_router_kernel(const float* __restrict_
     pdl_trigger();
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
-    float total = 0.f;
-    for (int k0 = 0; k0 < H; k0 += RT_KC) {
-        __syncthreads();
-        // stage x[t0..t0+7][k0..k0+255] and R[e0..e0+31][k0..k0+255] (float4s)
+    const int nchunk = H / RT_KC;
+    // x[t0..t0+7][k0..k0+255] and R[e0..e0+31][k0..k0+255] of chunk c into stage b
+    auto stage = [&](int c, int b) {
+        float* sx = rt_smem + b * RT_STAGE;
+        float* sr = sx + RT_TOK * RT_KC;
+        const int k0 = c * RT_KC;
         for (int i = tid; i < RT_TOK * RT_KC / 4; i += 256) {
             const int r = i / (RT_KC / 4), c4 = i % (RT_KC / 4);
             const int tt = min(t0 + r, T - 1);
-            reinterpret_cast<float4*>(&sx[r][0])[c4] =
-                __ldcg(reinterpret_cast<const float4*>(X + static_cast<int64_t>(tt) * H + k0) + c4);
+            cp_async16_cg(sx + r * RT_KC + 4 * c4, X + static_cast<int64_t>(tt) * H + k0 + 4 * c4);
         }
         for (int i = tid; i < 32 * RT_KC / 4; i += 256) {
             const int r = i / (RT_KC / 4), c4 = i % (RT_KC / 4);
             const int ee = min(e0 + r, E - 1);
-            reinterpret_cast<float4*>(&sr[r][0])[c4] =
-                __ldg(reinterpret_cast<const float4*>(R + static_cast<int64_t>(ee) * H + k0) + c4);
+            cp_async16_cg(sr + r * RT_LD + 4 * c4, R + static_cast<int64_t>(ee) * H + k0 + 4 * c4);
+        }
+        cp_async_commit();
+    };
+    stage(0, 0);
+    float total = 0.f;
+    for (int c = 0; c < nchunk; ++c) {
+        // stage (c + 1) & 1 was last read in step c - 1, which every thread has
+        // left (the barrier at its end)
+        if (c + 1 < nchunk) {
+            stage(c + 1, (c + 1) & 1);
+            cp_async_wait_group<1>();
+        } else {
+            cp_async_wait_group<0>();
         }
         __syncthreads();
+        const float* sx = rt_smem + (c & 1) * RT_STAGE;
+        const float* sr = sx + RT_TOK * RT_KC;
         float mid = 0.f;
-        const float4* xr = reinterpret_cast<const float4*>(&sx[warp][0]);
-        const float4* rr = reinterpret_cast<const float4*>(&sr[lane][0]);
+        const float4* xr = reinterpret_cast<const float4*>(sx + warp * RT_KC);
+        const float4* rr = reinterpret_cast<const float4*>(sr + lane * RT_LD);
 #pragma unroll 4
         for (int k16 = 0; k16 < RT_KC / 16; ++k16) {
             float lo = 0.f;
@@ -99,6 +129,7 @@ __global__ void __launch_bounds__(256) pf_router_kernel(const float* __restrict_
             mid += lo;
         }
         total += mid;
+        __syncthreads();
     }
     if (t < T && e < E) logits[static_cast<int64_t>(t) * E + e] = total;
 }
@@ -168,24 +199,25 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) zall += __shfl_xor_sync(0xffffffffu, zall, o);
     }
-    if (lane == 0) {
+    {
+        // lane s < K takes slot s: its weight, its outputs, and its append to
+        // the expert's list (the K appends in flight at once)
         const float lmax = s_l[warp][0];
         const bool degen = route_degenerate(lmax);  // route 0..K-1, NaN weights
-        bool bad = false;
-        float p[16], z = 0.f;
-        for (int s = 0; s < K; ++s) {
-            p[s] = expf(s_l[warp][s] - lmax);
-            z += p[s];
-        }
+        const float pr = lane < K ? expf(s_l[warp][lane] - lmax) : 0.f;
+        float z = pr;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         const float inv = 1.0f / (renorm ? z : zall);
-        for (int s = 0; s < K; ++s) {
-            int e = route_clamp(s_idx[warp][s], E, &bad);
-            float w = p[s] * inv;
+        bool bad = false;
+        if (lane < K) {
+            int e = route_clamp(s_idx[warp][lane], E, &bad);
+            float w = pr * inv;
             if (degen) {
-                e = s;
+                e = lane;
                 w = __int_as_float(0x7FC00000);
             }
-            const int64_t pair = static_cast<int64_t>(t) * K + s;
+            const int64_t pair = static_cast<int64_t>(t) * K + lane;
             tidx[pair] = e;
             tw[pair] = w;
             if (user_idx) user_idx[pair] = e;
@@ -193,7 +225,7 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(
             const int pos = atomicAdd(&cnt[e], 1);
             list[static_cast<int64_t>(e) * T + pos] = static_cast<int32_t>(pair);
         }
-        if (bad) record_error(err, DEV_ROUTE_RANGE);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(err, DEV_ROUTE_RANGE);
     }
     // x -> f16 with a power-of-two scale
     const float4* x4 = reinterpret_cast<const float4*>(X + static_cast<int64_t>(t) * H);

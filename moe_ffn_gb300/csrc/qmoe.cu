@@ -759,8 +759,25 @@ static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
     float* a = reinterpret_cast<float*>(w + L.a);
     const int T = s.n_tokens, H = s.hidden, E = s.num_experts, K = s.top_k, F = s.expert_dim;
 
+    static int configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!configured[dev & 63]) {
+        cudaError_t ce = cudaFuncSetAttribute(pf::pf_router_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              pf::RT_SMEM);
+        if (ce == cudaSuccess)
+            ce = cudaFuncSetAttribute(pf::pf_gateup_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, pf::GU_SMEM);
+        if (ce == cudaSuccess)
+            ce = cudaFuncSetAttribute(pf::pf_down_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, pf::DN_SMEM);
+        if (ce != cudaSuccess) return cuda_fail(ce, "cudaFuncSetAttribute(prefill)");
+        configured[dev & 63] = 1;
+    }
     cudaError_t e = launch_pdl(pf::pf_router_kernel, dim3((T + 7) / 8, (E + 31) / 32), dim3(256),
-                               0, st, router_W, x, T, H, E, logits, cnt);
+                               static_cast<size_t>(pf::RT_SMEM), st, router_W, x, T, H, E, logits,
+                               cnt);
     if (e != cudaSuccess) return cuda_fail(e, "pf_router launch");
     const int renorm = (s.route_flags & QMOE_ROUTE_NO_RENORM) ? 0 : 1;
     e = launch_pdl(pf::pf_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st,
@@ -768,18 +785,6 @@ static qmoe_status run_prefill(const float* router_W, const void* gate_stack,
                    topk_w, cnt, list, x16, xinv, d.err);
     if (e != cudaSuccess) return cuda_fail(e, "pf_topk launch");
 
-    static int configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!configured[dev & 63]) {
-        e = cudaFuncSetAttribute(pf::pf_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 pf::GU_SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(pf::pf_down_kernel,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, pf::DN_SMEM);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
-        configured[dev & 63] = 1;
-    }
     pf::PfParams pg = {};
     pg.W0 = static_cast<const uint8_t*>(gate_stack);
     pg.W1 = static_cast<const uint8_t*>(up_stack);
