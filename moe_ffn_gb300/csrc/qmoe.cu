@@ -162,11 +162,10 @@ static bool plan(StreamParams& p, int smem_optin, int smem_pair, int grid, int* 
     p.nstages = 0;
     const int fixed0 = smem_layout(p).total;
     // A CTA with a single tile gains nothing from a ring: one stage then
-    // holds the whole tile (whole rows, so few and large copies).  Where that
-    // stage fits in smem_pair bytes, two CTAs share an SM: the next launch's
-    // CTAs then stream their weights while this launch still computes.
-    // Otherwise the stage budget is at most 96 KB, and two stages must fit
-    // beside the x table.
+    // holds the whole tile (whole rows, so few and large copies), planned
+    // first within smem_pair bytes (half the SM's shared memory), else within
+    // the opt-in maximum.  Otherwise the stage budget is at most 96 KB, and
+    // two stages must fit beside the x table.
     const int64_t per_cta = (p.units + grid - 1) / grid;
     const bool one_tile = per_cta <= G::TU;
     if (one_tile) {
@@ -209,8 +208,8 @@ static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st)
     cudaGetDevice(&dev);
     if (smem > configured_smem[dev & 63]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        // the whole unified L1 as shared memory: two CTAs of this kernel, or
-        // of two consecutive launches, can then share an SM
+        // the whole unified L1 as shared memory: this launch's CTAs and the
+        // next launch's can then share an SM where their registers allow
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);

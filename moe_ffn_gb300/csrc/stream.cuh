@@ -726,19 +726,16 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
     return ok;
 }
 
-// QMV launches are bounded to two CTAs per SM (96 registers with nine warps
-// per CTA: the register file is split between the four sub-partitions), so
-// the next launch's CTAs can stream their weights beside this one.  Q6_K and
-// Q8_0 need more registers than that without spilling (and a 4096-wide
-// Q8_0 tile does not fit two per SM anyway): they keep one per SM.
+// One CTA per SM, with the registers the decode wants (92-168).  Bounding
+// the small formats to two CTAs per SM (96 registers: nine warps, the
+// register file split between four sub-partitions) lets the next launch of
+// the same kernel stream its weights beside this one, which helps only when
+// the same GEMV repeats back to back; between different kernels (the mixed
+// format sweep, a model's layers) the lower register budget costs more in
+// decode speed than the overlap gives (measured: sweep 38.9 -> 33.5 us per
+// step without the bound).
 template <class Fmt, int MODE>
-constexpr int stream_min_blocks() {
-    return (MODE == MODE_QMV && Fmt::SBB != 210 && Fmt::SBB != 272) ? 2 : 1;
-}
-
-template <class Fmt, int MODE>
-__global__ void __launch_bounds__(NTHREADS, (stream_min_blocks<Fmt, MODE>())) stream_gemv_kernel(
-    const StreamParams p) {
+__global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = smem_layout(p);
     Ring ring;
