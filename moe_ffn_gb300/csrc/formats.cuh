@@ -377,22 +377,6 @@ struct FmtQ6K {
     __device__ __forceinline__ static void dotR(const uint8_t* const (&sb)[R], int q,
                                                 const float4* __restrict__ xg, const float* xs16,
                                                 const float* sx, int nblk, float (&acc)[R]) {
-        if constexpr (R == 4) {
-            // four rows' words at once exceed the register budget: two
-            // passes of two rows, the second's loads after the first's
-            // arithmetic
-            const uint8_t* const s0[2] = {sb[0], sb[1]};
-            const uint8_t* const s1[2] = {sb[2], sb[3]};
-            float a0[2] = {acc[0], acc[1]}, a1[2] = {acc[2], acc[3]};
-            dotR<2>(s0, q, xg, xs16, sx, nblk, a0);
-            asm volatile("" ::: "memory");
-            dotR<2>(s1, q, xg, xs16, sx, nblk, a1);
-            acc[0] = a0[0];
-            acc[1] = a0[1];
-            acc[2] = a1[0];
-            acc[3] = a1[1];
-            return;
-        }
         const int h = q >> 1, c = q & 1;
         uint32_t A[R][4], B[R][4], H[R][4], S[R][2], db[R];
         float sc[R][4], d[R];
