@@ -212,7 +212,8 @@ size_t moe_ffn_workspace_size(const qmoe_moe_shape* shape);
  * decoded weights are nearly all below 2^-14; the single-token and
  * small-batch paths (f32 throughout) have neither term.  A decoded gate/up
  * weight beyond f16's range is flagged (QMOE_ERR_UNSUPPORTED from
- * qmoe_device_status).  A single token runs one cooperative kernel (one CTA per SM):
+ * qmoe_device_status).
+ * A single token runs one cooperative kernel (one CTA per SM):
  * router GEMV, a grid barrier, routing in every CTA, the routed gate/up rows
  * and then the down rows streamed through one pipeline, a second grid barrier
  * before the down products.  2..31 tokens run in cooperative launches of up
