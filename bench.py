@@ -205,7 +205,7 @@ def run_ours(args, rank, world):
                       "frac": round(alg / us / 1e3 / peak, 3), "bytes": alg}
         del gf
     dom = max(per_fmt, key=lambda n: per_fmt[n]["us"])
-    traffic = load_traffic(f"stream_gemv_{dom}")
+    traffic = load_traffic(f"qmv_{dom}")
 
     # ---- end to end through the public API with host buffers: every step
     # copies x from pinned host memory, runs the five GEMVs and copies y
@@ -259,7 +259,7 @@ def run_ours(args, rank, world):
                                    "the median repetition",
                    "arithmetic": "GGUF blocks decoded exactly; f32 activations, f32 sums",
                    "parallelism": f"replicas{world}"},
-        "roofline": {"bound": "hbm", "kernel": f"stream_gemv_kernel<{dom}, QMV>",
+        "roofline": {"bound": "hbm", "kernel": f"qmv_tile_kernel<{dom}>",
                      "achieved": per_fmt[dom]["gbs"], "peak": peak, "unit": "GB/s",
                      "frac": per_fmt[dom]["frac"], "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"},

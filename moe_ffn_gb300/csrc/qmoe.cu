@@ -202,11 +202,14 @@ static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st)
         return fail(QMOE_ERR_UNSUPPORTED,
                     "K = %d x %d groups of 256 does not fit the shared-memory pipeline",
                     p.n_kseg, p.nb_seg);
-    auto kern = stream_gemv_kernel<Fmt, MODE>;
-    static int configured_smem[64] = {};  // per instantiation and device
+    // QMV whose rows fit one stage: the eight-warp kernel (two CTAs per SM
+    // by registers)
+    const bool tile8 = MODE == MODE_QMV && p.nstages == 1;
+    auto kern = tile8 ? qmv_tile_kernel<Fmt> : stream_gemv_kernel<Fmt, MODE>;
+    static int configured_smem[2][64] = {};  // per instantiation, kernel and device
     int dev = 0;
     cudaGetDevice(&dev);
-    if (smem > configured_smem[dev & 63]) {
+    if (smem > configured_smem[tile8][dev & 63]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         // the whole unified L1 as shared memory: this launch's CTAs and the
         // next launch's can then share an SM where their registers allow
@@ -214,11 +217,11 @@ static qmoe_status run_stream(StreamParams p, const DevInfo& d, cudaStream_t st)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        configured_smem[dev & 63] = smem;
+        configured_smem[tile8][dev & 63] = smem;
     }
     p.err = d.err;
-    cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NTHREADS),
-                               static_cast<size_t>(smem), st, p);
+    cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)),
+                               dim3(tile8 ? NCW * 32 : NTHREADS), static_cast<size_t>(smem), st, p);
     if (e != cudaSuccess) return cuda_fail(e, "stream_gemv launch");
     return QMOE_OK;
 }

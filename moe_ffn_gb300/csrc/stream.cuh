@@ -726,14 +726,10 @@ __device__ bool consume_phase(const StreamParams& p, const Ring& ring, const int
     return ok;
 }
 
-// One CTA per SM, with the registers the decode wants (92-168).  Bounding
-// the small formats to two CTAs per SM (96 registers: nine warps, the
-// register file split between four sub-partitions) lets the next launch of
-// the same kernel stream its weights beside this one, which helps only when
-// the same GEMV repeats back to back; between different kernels (the mixed
-// format sweep, a model's layers) the lower register budget costs more in
-// decode speed than the overlap gives (measured: sweep 38.9 -> 33.5 us per
-// step without the bound).
+// Producer warp + eight consumer warps over a ring of stages: the phases of
+// the fused and batched kernels, MoE and dense GATEUP/DOWN launches, and QMV
+// when a CTA's rows span several stages (large GEMVs).  One CTA per SM.
+// (QMV rows that fit one stage run qmv_tile_kernel below.)
 template <class Fmt, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -799,6 +795,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) stream_gemv_kernel(const StreamPa
     named_bar(1, NCW * 32);
     if (!p.moe) named_bar(2, NTHREADS);  // the stage barriers are initialised
     consume_phase<Fmt, MODE>(p, ring, s_idx, s_w, xq, xs, part, ubeg, uend, it, tid);
+}
+
+// QMV with one tile per CTA (the plan's single stage holds all of the CTA's
+// rows): eight consumer warps, the first of which issues the tile's copies
+// before the dependency wait, so no warp is only a producer.  At 256
+// threads and at most 128 registers (every format's decode fits without
+// spilling), any two of these kernels fit one SM's register file, so the
+// next launch's CTAs - the same GEMV or another format's - stream their
+// weights beside this launch's wherever shared memory allows.  Measured on
+// the mixed-format sweep: 33.2 -> 30.9 us per step; a Q8_0 instance given
+// its own 149 registers blocks that pairing and costs 8 us per step.
+template <class Fmt>
+__global__ void __launch_bounds__(NCW * 32, 2) qmv_tile_kernel(const StreamParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const SmemLayout L = smem_layout(p);
+    Ring ring;
+    ring.full = reinterpret_cast<uint64_t*>(smem + L.off_full);
+    ring.empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
+    ring.stages = smem + L.off_stage;
+    ring.nstages = 1;
+    ring.stage_bytes = p.stage_bytes;
+    int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.off_tidx);
+    float* s_w = reinterpret_cast<float*>(smem + L.off_tw);
+    float* part = reinterpret_cast<float*>(smem + L.off_part);
+    float* xs = reinterpret_cast<float*>(smem + L.off_xs);
+    float* xq = reinterpret_cast<float*>(smem + L.off_xq);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int64_t ubeg, uend;
+    unit_range(p, static_cast<int>(blockIdx.x), ubeg, uend);
+    if (tid == 0) {
+        mbar_init(&ring.full[0], 1);
+        mbar_init(&ring.empty[0], NCW);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int itp = 0;
+        produce_phase<Fmt, MODE_QMV>(p, ring, s_idx, ubeg, uend, itp, lane);
+    }
+    pdl_wait();
+    pdl_trigger();
+    build_xprime<Fmt>(p.x, p.nb_seg,
+                      p.tail ? (p.nb_seg - 1) * 16 + 2 * p.tail : p.nb_seg * 16, xq, xs, tid,
+                      NCW * 32, p.err);
+    named_bar(1, NCW * 32);
+    int it = 0;
+    consume_phase<Fmt, MODE_QMV>(p, ring, s_idx, s_w, xq, xs, part, ubeg, uend, it, tid);
 }
 
 // ------------------------------------------------------------ host planning
