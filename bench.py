@@ -561,12 +561,12 @@ ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "A
              "0xd49": "Arm Neoverse N2", "0xd8f": "Arm Neoverse V3"}
 
 
-def cpu_model():
+def cpu_model(cpuinfo="/proc/cpuinfo"):
     """The host CPU's name: x86 'model name', or an Arm core's part number
     with its name when known (e.g. 0xd4f, Neoverse V2 as in Grace)."""
     part = None
     try:
-        for line in open("/proc/cpuinfo"):
+        for line in open(cpuinfo):
             k, _, v = line.partition(":")
             k, v = k.strip(), v.strip()
             if k in ("model name", "Model name"):
